@@ -1,0 +1,67 @@
+"""Seeded synthetic inputs for ring attention workloads.
+
+This module only draws random numbers; it contains none of the attention
+arithmetic.  Both the CUDA path's tests/bench and the CPU oracle consume the
+tensors it returns, so the two sides see bit-identical inputs.
+
+Recipe (fixed, so that every caller reproduces the same values):
+  * one ``torch.Generator('cpu')`` seeded with ``seed``;
+  * tensors drawn in the order Q, K, V, dO (dO only when requested);
+  * inside a tensor, one ``randn(S, D)`` float32 draw per (b, h) slab, in
+    row-major (b, h) order;
+  * each slab is multiplied by ``scale`` (0.5 for the 131072-token workload:
+    a power of two, so the product is exact) and then rounded to the storage
+    dtype with round-to-nearest-even (``Tensor.to``).
+
+The tensors are in *storage order* [B, H, S, D]: for the striped layout,
+storage row ``p = i*c + r`` of a head holds token ``r*N + i``; the generator
+does not care, it only fills storage rows.
+"""
+from __future__ import annotations
+
+import torch
+
+_DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def make_inputs(B: int, H: int, S: int, D: int, seed: int, *, dtype: str = "bf16",
+                scale: float = 1.0, with_grad: bool = False) -> dict:
+    """Return {'q','k','v'[, 'do']} CPU tensors of shape [B, H, S, D]."""
+    if dtype not in _DTYPES:
+        raise ValueError(f"dtype must be one of {sorted(_DTYPES)}")
+    tdt = _DTYPES[dtype]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    names = ["q", "k", "v"] + (["do"] if with_grad else [])
+    out = {}
+    for name in names:
+        t = torch.empty((B, H, S, D), dtype=tdt)
+        for b in range(B):
+            for h in range(H):
+                x = torch.randn((S, D), generator=g, dtype=torch.float32)
+                if scale != 1.0:
+                    x.mul_(scale)
+                t[b, h].copy_(x.to(tdt))
+        out[name] = t
+    return out
+
+
+def as_float64(t: torch.Tensor):
+    """Upcast a CPU tensor (bf16 or f32) to a float64 NumPy array, exactly."""
+    return t.to(torch.float64).numpy()
+
+
+# The five workloads the library is specified against.  Names say what each
+# is; sizes are the workload's own.  ``seed`` is the workload's 1-based index.
+WORKLOADS = {
+    "tiny_f32": dict(B=1, H=1, S=256, D=64, N=4, causal=False, layout="contiguous",
+                     dtype="f32", scale=1.0, seed=1, grad=False),
+    "causal_8k": dict(B=1, H=8, S=8192, D=128, N=8, causal=True, layout="contiguous",
+                      dtype="bf16", scale=1.0, seed=2, grad=False),
+    "balance_32k": dict(B=1, H=16, S=32768, D=128, N=16, causal=True, layout="striped",
+                        dtype="bf16", scale=1.0, seed=3, grad=False),
+    "long_128k": dict(B=1, H=32, S=131072, D=128, N=32, causal=True, layout="contiguous",
+                      dtype="bf16", scale=0.5, seed=4, grad=False),
+    "fwdbwd_64k": dict(B=1, H=32, S=65536, D=128, N=16, causal=True, layout="striped",
+                       dtype="bf16", scale=1.0, seed=5, grad=True),
+}

@@ -1,0 +1,345 @@
+"""Pins for the CPU oracle: what the pages and the mathematics fix, not the
+oracle restated.  CPU only (no gpu marker)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as orc
+
+LAYOUTS = ["contiguous", "striped"]
+
+
+def _rand(rng, *shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- brute force
+def _brute_force_head(q, k, v, N, causal, striped):
+    """Scalar Python loops: softmax without max subtraction, direct sums.
+
+    Token of storage row p: row r of block i is token i*c+r (contiguous) or
+    r*N+i (striped) -- written here independently of the oracle.
+    """
+    S, D = len(q), len(q[0])
+    c = S // N
+
+    def tok(p):
+        i, r = p // c, p % c
+        return r * N + i if striped else p
+
+    O, L = [], []
+    for a in range(S):
+        w = []
+        for b in range(S):
+            if causal and tok(b) > tok(a):
+                w.append(0.0)
+                continue
+            dot = sum(q[a][x] * k[b][x] for x in range(D))
+            w.append(math.exp(dot / math.sqrt(D)))
+        tot = sum(w)
+        O.append([sum(w[b] * v[b][x] for b in range(S)) / tot for x in range(D)])
+        L.append(math.log(tot))
+    return np.array(O), np.array(L)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S,N,D", [(8, 2, 4), (12, 3, 5), (16, 4, 8), (6, 1, 3)])
+def test_brute_force_matches_both_forms(S, N, D, causal, layout):
+    rng = np.random.default_rng(S * 100 + N * 10 + D + causal)
+    q, k, v = (_rand(rng, 1, 1, S, D) for _ in range(3))
+    ob, lb = _brute_force_head(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), N, causal,
+                               layout == "striped")
+    on, ln = orc.naive_attention(q, k, v, N, causal, layout)
+    orr, lr = orc.ring_attention(q, k, v, N, causal, layout)
+    np.testing.assert_allclose(on[0, 0], ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ln[0, 0], lb, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(orr[0, 0], ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lr[0, 0], lb, rtol=0, atol=1e-12)
+
+
+def test_demo_setup_of_the_explainer_agrees():
+    """[AQ] §Python 演示: n=16, d=8, 4 devices, seed 42; the page expects the
+    ring result to equal full attention for every device.  It prints no
+    values, so this pin is agreement only."""
+    np.random.seed(42)
+    n, d, ndev = 16, 8, 4
+    Q = np.random.randn(n, d)
+    K = np.random.randn(n, d)
+    V = np.random.randn(n, d)
+    on, _ = orc.naive_attention(Q[None, None], K[None, None], V[None, None], ndev, False, "contiguous")
+    b = n // ndev
+    for dev in range(ndev):
+        o, _ = orc.ring_block_attention(Q, K, V, dev, ndev, False, "contiguous")
+        assert np.abs(o - on[0, 0, dev * b:(dev + 1) * b]).max() < 1e-14
+
+
+# --------------------------------------------------------------- page fixtures
+def test_striped_assignment_matches_page(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "striped_tokens_n4.json")))
+    pos = orc.token_positions(g["S"], g["N"], "striped")
+    c = g["S"] // g["N"]
+    for i, toks in enumerate(g["tokens_per_device"]):
+        assert pos[i * c:(i + 1) * c].tolist() == toks
+
+
+def test_ring_order_matches_diagram(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "ring_diagram_n4.json")))
+    N = g["N"]
+    for step, held in g["block_held_at_step"].items():
+        assert [orc.ring_order(i, N)[int(step)] for i in range(N)] == held
+    # one step later, host (i+1) holds what host i held: i sends to i+1
+    for i in range(N):
+        dst = g["sends_to"][i]
+        assert orc.ring_order(dst, N)[1] == orc.ring_order(i, N)[0]
+
+
+def test_causal_block_work_matches_page(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "causal_work_100tok_n4.json")))
+    w = orc.block_rectangle_work(g["S"], g["N"], g["layout"], g["causal"])
+    assert w.tolist() == g["block_rectangle_work"]
+    assert w[-1] // w[0] == g["ratio_last_to_first"]
+
+
+def test_flop_convention_matches_pages(golden_dir):
+    from ring_attention_fwd_gb300 import flops
+    g = json.load(open(os.path.join(golden_dir, "block_pair_cost.json")))
+    for case in g["cases"]:
+        c, d = case["c"], case["d"]
+        # one query block against one KV block, no mask: a 1-block sequence
+        assert flops.fwd_flops(B=1, H=1, S=c, D=d, causal=False) == case["flops"]
+        assert flops.kv_block_bytes(c, d) == case["kv_bytes"]
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_equal_keys_give_prefix_mean(layout):
+    """All keys equal -> uniform weights over the visible set: O(t) is the mean
+    of the visible values and LSE = ln|visible| + s."""
+    rng = np.random.default_rng(7)
+    S, N, D = 24, 4, 6
+    q = _rand(rng, 1, 1, S, D)
+    krow = _rand(rng, D)
+    k = np.broadcast_to(krow, (1, 1, S, D)).copy()
+    v = _rand(rng, 1, 1, S, D)
+    o, lse = orc.ring_attention(q, k, v, N, True, layout)
+    pos = orc.token_positions(S, N, layout)
+    by_token = np.empty((S, D))
+    by_token[pos] = v[0, 0]
+    for p in range(S):
+        t = pos[p]
+        np.testing.assert_allclose(o[0, 0, p], by_token[:t + 1].mean(axis=0), atol=1e-13)
+        s = q[0, 0, p] @ krow / math.sqrt(D)
+        assert abs(lse[0, 0, p] - (math.log(t + 1) + s)) < 1e-12
+
+
+def test_zero_queries_non_causal_mean_and_log_count():
+    rng = np.random.default_rng(8)
+    S, N, D = 20, 5, 4
+    q = np.zeros((1, 1, S, D))
+    k, v = _rand(rng, 1, 1, S, D), _rand(rng, 1, 1, S, D)
+    o, lse = orc.naive_attention(q, k, v, N, False, "contiguous")
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0].mean(axis=0), (S, D)), atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(S), atol=1e-14)
+
+
+def test_equal_values_give_that_value():
+    rng = np.random.default_rng(9)
+    S, N, D = 16, 4, 5
+    q, k = _rand(rng, 1, 1, S, D, scale=3.0), _rand(rng, 1, 1, S, D, scale=3.0)
+    u = _rand(rng, D)
+    v = np.broadcast_to(u, (1, 1, S, D)).copy()
+    for layout in LAYOUTS:
+        o, _ = orc.ring_attention(q, k, v, N, True, layout)
+        np.testing.assert_allclose(o[0, 0], np.broadcast_to(u, (S, D)), atol=1e-13)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_first_token_sees_only_itself(layout):
+    """Causal token 0 has a single visible key: O = v_0, LSE = q_0.k_0/sqrt(D)."""
+    rng = np.random.default_rng(10)
+    S, N, D = 16, 4, 8
+    q, k, v = (_rand(rng, 1, 1, S, D) for _ in range(3))
+    o, lse = orc.ring_attention(q, k, v, N, True, layout)
+    p0 = int(np.where(orc.token_positions(S, N, layout) == 0)[0][0])
+    np.testing.assert_allclose(o[0, 0, p0], v[0, 0, p0], atol=1e-15)
+    assert abs(lse[0, 0, p0] - q[0, 0, p0] @ k[0, 0, p0] / math.sqrt(D)) < 1e-14
+
+
+def test_single_block_ring_is_plain_softmax():
+    rng = np.random.default_rng(11)
+    q, k, v = (_rand(rng, 2, 2, 10, 4) for _ in range(3))
+    for causal in (False, True):
+        a = orc.ring_attention(q, k, v, 1, causal, "contiguous")
+        b = orc.naive_attention(q, k, v, 1, causal, "striped")   # N=1: same map
+        np.testing.assert_allclose(a[0], b[0], atol=1e-14)
+        np.testing.assert_allclose(a[1], b[1], atol=1e-14)
+
+
+# ------------------------------------------------------------------ invariants
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_order_invariance(layout, causal):
+    """Any permutation of the KV blocks gives the same result ([FT] core
+    insight; [CH] §4 first assumption)."""
+    rng = np.random.default_rng(12)
+    S, N, D = 48, 6, 8
+    q, k, v = (_rand(rng, 1, 2, S, D, scale=2.0) for _ in range(3))
+    ref = orc.ring_attention(q, k, v, N, causal, layout)
+    for seed in range(4):
+        perm_rng = np.random.default_rng(100 + seed)
+        out = orc.ring_attention(q, k, v, N, causal, layout,
+                                 order_fn=lambda i, n: list(perm_rng.permutation(n)))
+        np.testing.assert_allclose(out[0], ref[0], atol=1e-13)
+        np.testing.assert_allclose(out[1], ref[1], atol=1e-13)
+
+
+def test_merge_of_key_halves_equals_whole():
+    """Split the keys into two disjoint sets, attend to each, merge: equals
+    attention over all keys ([FT] "Online Softmax" merge identity)."""
+    rng = np.random.default_rng(13)
+    S, D = 40, 8
+    q, k, v = (_rand(rng, S, D, scale=2.0) for _ in range(3))
+    whole_o, whole_l = orc.attention_rows(q, k, v, np.arange(S), 1, False, "contiguous")
+    sel = rng.permutation(S)
+    A, B = sel[:13], sel[13:]
+    oa, la = orc.attention_rows(q, k[A], v[A], np.arange(S), 1, False, "contiguous")
+    ob, lb = orc.attention_rows(q, k[B], v[B], np.arange(S), 1, False, "contiguous")
+    om, lm = orc.lse_merge(oa, la, ob, lb)
+    np.testing.assert_allclose(om, whole_o, atol=1e-13)
+    np.testing.assert_allclose(lm, whole_l, atol=1e-13)
+    # the denominators obey l = l1 e^{m1-m} + l2 e^{m2-m} with lse = m + ln l
+    assert np.allclose(np.exp(lm), np.exp(la) + np.exp(lb), rtol=1e-13)
+
+
+def test_merge_edge_cases():
+    o = np.arange(6.0).reshape(2, 3)
+    ninf = np.array([-np.inf, -np.inf])
+    om, lm = orc.lse_merge(o, ninf, 2 * o, ninf)
+    assert np.all(om == 0) and np.all(lm == -np.inf)
+    om, lm = orc.lse_merge(o, np.array([0.5, -1.0]), 2 * o, ninf)   # one side empty
+    np.testing.assert_allclose(om, o)
+    np.testing.assert_allclose(lm, [0.5, -1.0])
+    om, lm = orc.lse_merge(o, np.array([1e4, 0.0]), 2 * o, np.array([1e4, 0.0]))  # huge, equal
+    np.testing.assert_allclose(om, 1.5 * o)
+    np.testing.assert_allclose(lm, [1e4 + math.log(2), math.log(2)])
+
+
+def test_striped_equals_contiguous_after_unpermuting():
+    rng = np.random.default_rng(14)
+    S, N, D = 32, 4, 8
+    q, k, v = (_rand(rng, 1, 1, S, D) for _ in range(3))
+    pos = orc.token_positions(S, N, "striped")      # storage row -> token
+    # token-order tensors for the contiguous run
+    qt, kt, vt = (np.empty_like(x) for x in (q, k, v))
+    for src, dst in ((q, qt), (k, kt), (v, vt)):
+        dst[0, 0, pos] = src[0, 0]
+    os_, ls_ = orc.ring_attention(q, k, v, N, True, "striped")
+    oc, lc = orc.ring_attention(qt, kt, vt, N, True, "contiguous")
+    np.testing.assert_allclose(os_[0, 0], oc[0, 0, pos], atol=1e-13)
+    np.testing.assert_allclose(ls_[0, 0], lc[0, 0, pos], atol=1e-13)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_causal_future_keys_do_not_leak(layout):
+    rng = np.random.default_rng(15)
+    S, N, D = 32, 4, 4
+    q, k, v = (_rand(rng, 1, 1, S, D) for _ in range(3))
+    pos = orc.token_positions(S, N, layout)
+    o1, l1 = orc.ring_attention(q, k, v, N, True, layout)
+    cut = 20
+    fut = pos > cut
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0, fut] += 5.0
+    v2[0, 0, fut] -= 3.0
+    o2, l2 = orc.ring_attention(q, k2, v2, N, True, layout)
+    keep = pos <= cut
+    np.testing.assert_array_equal(o1[0, 0, keep], o2[0, 0, keep])
+    np.testing.assert_array_equal(l1[0, 0, keep], l2[0, 0, keep])
+    assert not np.allclose(o1[0, 0, ~keep], o2[0, 0, ~keep])
+
+
+def test_probability_rows_sum_to_one():
+    rng = np.random.default_rng(16)
+    S, N, D = 24, 3, 8
+    q, k, v = (_rand(rng, S, D, scale=2.0) for _ in range(3))
+    for layout in LAYOUTS:
+        _, lse = orc.attention_rows(q, k, v, np.arange(S), N, True, layout)
+        P = orc.attention._probabilities(q, k, lse, N, True, layout)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-14)
+
+
+# ------------------------------------------------------------------- gradients
+def _loss(q, k, v, do, N, causal, layout):
+    o, _ = orc.naive_attention(q, k, v, N, causal, layout)
+    return float((o * do).sum())
+
+
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("contiguous", False)])
+def test_backward_matches_finite_differences(layout, causal):
+    rng = np.random.default_rng(17)
+    S, N, D = 12, 3, 4
+    q, k, v, do = (_rand(rng, 1, 1, S, D) for _ in range(4))
+    o, lse = orc.naive_attention(q, k, v, N, causal, layout)
+    dq, dk, dv = orc.attention_bwd(q, k, v, o, lse, do, N, causal, layout)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            fp = _loss(args["q"], args["k"], args["v"], do, N, causal, layout)
+            args[name] = xm
+            fm = _loss(args["q"], args["k"], args["v"], do, N, causal, layout)
+            num[idx] = (fp - fm) / (2 * h)
+        np.testing.assert_allclose(g, num, atol=2e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_backward_sum_identities(layout):
+    """Rows of P sum to 1 and rows of dS sum to 0, hence per head
+    sum_k dK = 0 and sum_k dV = sum_q dO."""
+    rng = np.random.default_rng(18)
+    S, N, D = 64, 4, 16
+    q, k, v, do = (_rand(rng, 1, 2, S, D) for _ in range(4))
+    o, lse = orc.naive_attention(q, k, v, N, True, layout)
+    dq, dk, dv = orc.attention_bwd(q, k, v, o, lse, do, N, True, layout)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+
+
+def test_dq_rows_match_full_backward():
+    rng = np.random.default_rng(19)
+    S, N, D = 40, 4, 8
+    q, k, v, do = (_rand(rng, S, D) for _ in range(4))
+    for layout in LAYOUTS:
+        o, lse = orc.attention_rows(q, k, v, np.arange(S), N, True, layout)
+        dq, _, _ = orc.attention_bwd_head(q, k, v, o, lse, do, N, True, layout)
+        rows = np.array([0, 7, 13, 39])
+        np.testing.assert_allclose(orc.attention_bwd_dq_rows(q, k, v, do, rows, N, True, layout),
+                                   dq[rows], atol=1e-13)
+
+
+# ------------------------------------------------------------- work per device
+def test_visible_pairs_brute_force_and_balance():
+    for S, N in ((16, 4), (64, 8), (96, 3)):
+        for layout in LAYOUTS:
+            pos = orc.token_positions(S, N, layout)
+            vis = orc.visible(pos, pos, True)
+            brute = vis.sum(axis=1).reshape(N, S // N).sum(axis=1)
+            assert orc.visible_pairs_per_device(S, N, layout, True).tolist() == brute.tolist()
+            assert brute.sum() == S * (S + 1) // 2
+    # contiguous: device i does i*c^2 + c(c+1)/2; striped: N c(c-1)/2 + c(i+1)
+    S, N = 32768, 16
+    c = S // N
+    cont = orc.visible_pairs_per_device(S, N, "contiguous", True)
+    strp = orc.visible_pairs_per_device(S, N, "striped", True)
+    assert cont.tolist() == [i * c * c + c * (c + 1) // 2 for i in range(N)]
+    assert strp.tolist() == [N * c * (c - 1) // 2 + c * (i + 1) for i in range(N)]
+    assert cont.max() / cont.min() > 2 * N - 2 and strp.max() / strp.min() < 1.001
