@@ -1,0 +1,169 @@
+/*
+ * ringattn.h -- C ABI of libringattn.so: ring-order blockwise attention on one
+ * GB300 GPU (sm_103a).
+ *
+ * Pages this interface implements (title and section only):
+ *   [FT] "Ring Attention如何让大模型突破百万Token上下文：从环形通信到计算重叠的技术突围"
+ *        (answer.freetools.me)
+ *   [CH] "Ring Attention with Blockwise Transformers for Near Infinite Context",
+ *        reading notes on arXiv 2310.01889 (papers.chlience.com)
+ *   [AQ] "Ring Attention" explainer (aiqz.cc)
+ *
+ * Common conventions
+ * ------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never frees or retains them; it allocates no device memory on any call
+ *    (the backward takes a caller-sized workspace).
+ *  - Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, S, D] in *storage
+ *    order*.  The sequence is cut into N equal blocks of c = S / N rows, one per
+ *    virtual ring host ([CH] §5.2).  Layout RA_CONTIGUOUS: storage row p holds
+ *    token p.  Layout RA_STRIPED: storage row p = i*c + r holds token r*N + i,
+ *    i.e. token t lives on block t mod N ([FT] "因果掩码的负载均衡挑战").
+ *  - LSE is float32 [B, H, S], storage order: LSE = ln sum_k exp(q.k / sqrt(D))
+ *    over the keys the row sees (natural log, scaled-score units).
+ *  - dtype RA_BF16: 16-bit bfloat16 tensors, float32 accumulation, outputs
+ *    rounded to nearest even.  dtype RA_F32: float32 tensors throughout.
+ *  - Causal masking is per token (key token <= query token, [AQ] §工程实现);
+ *    with the contiguous layout whole KV blocks j > i are skipped.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream).  Argument errors are detected on the host before any
+ *    launch and return synchronously; output contents are then unchanged.
+ *    After a launched call fails, output contents are unspecified.
+ *  - Return value: an ra_status.  ra_last_error() gives a message for the most
+ *    recent non-OK status of the calling thread.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RA_API __attribute__((visibility("default")))
+#else
+#define RA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_ARG = 1,          /* bad pointer, size, alignment or enum value   */
+  RA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+  RA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed  */
+  RA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out           */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+typedef enum { RA_CONTIGUOUS = 0, RA_STRIPED = 1 } ra_layout;
+
+/*
+ * ra_fwd -- forward pass: O = softmax(Q K^T / sqrt(D)) V and its LSE.
+ *
+ * Each query block i sweeps the KV blocks in ring order j = i, i-1, ... mod N
+ * ([FT] "Ring Attention的核心洞察" step 3; [AQ] §环状拓扑) and folds every
+ * score tile S_ij = Q_i K_j^T / sqrt(D) into per-row online-softmax state
+ * (running max m, denominator l, unnormalised numerator O) ([AQ] §分块注意力,
+ * the m / l / O update equations; [FT] "Online Softmax").  At the end
+ * O <- O / l and LSE <- m + ln l.
+ *
+ *   Q, K, V : [B,H,S,D] of `dtype`, 16-byte aligned.
+ *   O       : [B,H,S,D] of `dtype` (output), 16-byte aligned.
+ *   LSE     : [B,H,S] float32 (output), 4-byte aligned.
+ *   B, H, S, D, N : B,H >= 1; S >= 1 with S % N == 0; N >= 1.
+ *                   RA_BF16 requires D == 128.  RA_F32 requires D % 4 == 0
+ *                   and D <= 128.  Any block length c = S/N is accepted
+ *                   (a partial last tile is masked).
+ *   causal  : 0 or 1.   layout : ra_layout.   dtype : ra_dtype.
+ *   stream  : cudaStream_t.
+ * Errors: RA_ERR_ARG (null pointer, misalignment, S % N != 0, sizes <= 0,
+ * bad enum, B*H*S*D overflowing int64, or B*H or S beyond 2^31-1),
+ * RA_ERR_UNSUPPORTED (D outside the list above), RA_ERR_CUDA.
+ */
+RA_API int ra_fwd(const void* Q, const void* K, const void* V,
+           int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+           int causal, int layout, int dtype,
+           void* O, float* LSE, void* stream);
+
+/*
+ * ra_merge -- LogSumExp merge of two partial states over disjoint key sets,
+ * in place into (O_a, lse_a)  ([FT] "Online Softmax": l = l1 e^{m1-m} +
+ * l2 e^{m2-m} and its log-space form).  Per row:
+ *     M = max(lse_a, lse_b);  lse = M + ln(e^{lse_a-M} + e^{lse_b-M});
+ *     O_a <- e^{lse_a-lse} O_a + e^{lse_b-lse} O_b.
+ * Both lse -inf (no key seen on either side): lse = -inf and O = 0.
+ *
+ *   O_a : [rows, D] of `dtype` (in/out);   lse_a : [rows] float32 (in/out)
+ *   O_b : [rows, D] of `dtype` (in);       lse_b : [rows] float32 (in)
+ *   rows >= 0 (0 is a no-op), D in 1..1024.  Pointers 4-byte aligned (O_* of
+ *   bf16 may be 2-byte aligned).  O_a and O_b must not overlap unless equal.
+ * Errors: RA_ERR_ARG, RA_ERR_CUDA.
+ */
+RA_API int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b,
+             int64_t rows, int64_t D, int dtype, void* stream);
+
+/*
+ * ra_bwd_workspace_bytes -- size of the caller-allocated workspace ra_bwd
+ * needs for these sizes (float32 dQ accumulator [B,H,S,D] and the per-row
+ * D_vec = rowsum(dO * O) [B,H,S], each 256-byte aligned).  0 on bad sizes.
+ */
+RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * ra_bwd -- backward pass from the saved output and LSE.
+ *
+ * The pages state only that the backward re-sweeps the KV blocks along the
+ * ring to accumulate dQ, dK, dV from the saved softmax state ([CH] §5.2, last
+ * paragraph).  This computes the gradient of the forward's definition:
+ *     P = exp(Q K^T / sqrt(D) - LSE) on visible entries (0 elsewhere),
+ *     dV = P^T dO,  dP = dO V^T,  D_vec = rowsum(dO * O),
+ *     dS = P * (dP - D_vec),  dQ = dS K / sqrt(D),  dK = dS^T Q / sqrt(D).
+ * Each KV tile sweeps the query blocks that see it in ring order.
+ *
+ *   Q, K, V, O, dO : [B,H,S,D] inputs;  LSE [B,H,S] float32 input (as ra_fwd
+ *   wrote it).  dQ, dK, dV : [B,H,S,D] outputs of `dtype`.  16-byte aligned.
+ *   workspace : device memory of at least ra_bwd_workspace_bytes(...) bytes,
+ *   256-byte aligned; its contents on entry do not matter.
+ *   Sizes, causal, layout as for ra_fwd; RA_BF16 with D == 128 only.
+ * Errors: RA_ERR_ARG (also: workspace too small), RA_ERR_UNSUPPORTED,
+ * RA_ERR_CUDA.
+ */
+RA_API int ra_bwd(const void* Q, const void* K, const void* V, const void* O,
+           const float* LSE, const void* dO,
+           void* dQ, void* dK, void* dV,
+           int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+           int causal, int layout, int dtype,
+           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * ra_set_timing_buffer -- per-virtual-host time accounting for later bf16
+ * ra_fwd calls from any thread (process-wide setting; NULL disables).
+ * `dev_buf` is a caller-owned device array of n uint64 that the caller zeroes;
+ * a call with ring size N needs n >= N*N.  Entry [i*N + s] accumulates the
+ * nanoseconds (%globaltimer) that the kernel's CTAs spent on query block i's
+ * rows while processing ring step s (KV block (i - s) mod N).  This is the
+ * per-virtual-device time of [FT] "因果掩码的负载均衡挑战".
+ * Errors: RA_ERR_ARG (n < 1 with a non-NULL buffer).
+ */
+RA_API int ra_set_timing_buffer(uint64_t* dev_buf, size_t n);
+
+/*
+ * ra_check_device_status -- synchronise `stream`, then read and clear the
+ * library's device-side status word.  Returns RA_ERR_TIMEOUT if any kernel
+ * launched since the previous check gave up a bounded wait (the kernel then
+ * returned early and its outputs are unspecified), else RA_OK or RA_ERR_CUDA.
+ */
+RA_API int ra_check_device_status(void* stream);
+
+/* Message for the calling thread's most recent non-OK status ("" if none). */
+RA_API const char* ra_last_error(void);
+
+/* Library version string, e.g. "ringattn 0.1 sm_103a". */
+RA_API const char* ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RINGATTN_H */

@@ -2,6 +2,9 @@
 
 The compute lives in ``libringattn.so`` (C ABI, hand-written CUDA kernels);
 ``binding`` marshals arguments to it.  The library is loaded on first use and
-a missing or stale build raises immediately: there is no fallback path.
+a missing build raises immediately: there is no fallback path.
 """
 from . import flops, inputs  # noqa: F401
+from .binding import (  # noqa: F401
+    RingAttnError, bwd, bwd_workspace_bytes, check_device_status, fwd, merge, set_timing_buffer, version,
+)

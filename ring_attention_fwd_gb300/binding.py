@@ -1,0 +1,163 @@
+"""ctypes binding to libringattn.so -- argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  PyTorch is
+used for device allocation and the current stream; no function here computes
+attention values.  If the library is missing the first call raises
+``RuntimeError`` (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libringattn.so")
+_lib = None
+_lock = threading.Lock()
+
+RA_OK, RA_ERR_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
+RA_F32, RA_BF16 = 0, 1
+RA_CONTIGUOUS, RA_STRIPED = 0, 1
+_LAYOUT = {"contiguous": RA_CONTIGUOUS, "striped": RA_STRIPED}
+_DTYPE = {torch.float32: RA_F32, torch.bfloat16: RA_BF16}
+
+# exported symbol -> (restype, argtypes)
+_i64, _vp, _fp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "ra_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp, _vp]),
+    "ra_merge": (_int, [_vp, _fp, _vp, _fp, _i64, _i64, _int, _vp]),
+    "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                      _int, _int, _int, _vp, _sz, _vp]),
+    "ra_set_timing_buffer": (_int, [_vp, _sz]),
+    "ra_check_device_status": (_int, [_vp]),
+    "ra_last_error": (ctypes.c_char_p, []),
+    "ra_version": (ctypes.c_char_p, []),
+}
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"ringattn status {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """Load libringattn.so (once).  Raises RuntimeError if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with `python -m ring_attention_fwd_gb300.build` "
+                    "(there is no non-CUDA fallback)")
+            L = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != RA_OK:
+        raise RingAttnError(rc, lib().ra_last_error().decode())
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def fwd(q, k, v, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
+        o=None, lse=None, stream=None):
+    """Ring-order blockwise attention forward.  q, k, v: [B, H, S, D] CUDA
+    tensors (bf16 or f32) in storage order.  Returns (o, lse)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype)
+    if q.dtype not in _DTYPE:
+        raise ValueError("dtype must be bfloat16 or float32")
+    B, H, S, D = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _need(o, "o", q.dtype)
+    _need(lse, "lse", torch.float32)
+    _check(lib().ra_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, S, D, int(n_blocks),
+                        int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], o.data_ptr(), lse.data_ptr(),
+                        _stream_ptr(stream)))
+    return o, lse
+
+
+def merge(o_a, lse_a, o_b, lse_b, *, stream=None):
+    """In-place LogSumExp merge of (o_b, lse_b) into (o_a, lse_a)."""
+    _need(o_a, "o_a")
+    _need(o_b, "o_b", o_a.dtype)
+    _need(lse_a, "lse_a", torch.float32)
+    _need(lse_b, "lse_b", torch.float32)
+    D = o_a.shape[-1]
+    rows = o_a.numel() // D if D else 0
+    if lse_a.numel() != rows or lse_b.numel() != rows or o_b.numel() != o_a.numel():
+        raise ValueError("shape mismatch")
+    _check(lib().ra_merge(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(), lse_b.data_ptr(), rows, D,
+                          _DTYPE[o_a.dtype], _stream_ptr(stream)))
+    return o_a, lse_a
+
+
+def bwd_workspace_bytes(B, H, S, D) -> int:
+    return int(lib().ra_bwd_workspace_bytes(B, H, S, D))
+
+
+def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
+        dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward from the saved (o, lse).  Returns (dq, dk, dv)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _need(t, name, q.dtype)
+    _need(lse, "lse", torch.float32)
+    B, H, S, D = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, S, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib().ra_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, int(n_blocks),
+                        int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def set_timing_buffer(buf):
+    """Enable per-(virtual host, ring step) timing into a uint64/int64 CUDA
+    tensor of >= N*N entries (caller zeroes it); None disables."""
+    if buf is None:
+        _check(lib().ra_set_timing_buffer(None, 0))
+    else:
+        _need(buf, "timing buffer")
+        _check(lib().ra_set_timing_buffer(buf.data_ptr(), buf.numel()))
+
+
+def check_device_status(stream=None):
+    """Synchronise and raise RingAttnError(RA_ERR_TIMEOUT) if a kernel gave up
+    a bounded wait since the last check."""
+    _check(lib().ra_check_device_status(_stream_ptr(stream)))
+
+
+def version() -> str:
+    return lib().ra_version().decode()

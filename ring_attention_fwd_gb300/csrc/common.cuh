@@ -1,0 +1,172 @@
+// common.cuh -- shared by the kernels and the host library: the ring-order
+// work schedule, the per-element visibility rule, and launcher declarations.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ra {
+
+// Geometry of one call.  The sequence of S rows is cut into N blocks of
+// c = S/N rows (one per virtual ring host).  Storage row p = i*c + r is row r
+// of block i; for the striped layout it holds token r*N + i, for the
+// contiguous layout token p.
+struct RingGeom {
+  int N;        // ring size (blocks)
+  int c;        // rows per block
+  int causal;   // 0/1
+  int striped;  // 0 = contiguous, 1 = striped
+  int kt_w;     // rows per KV tile
+  int n_kt;     // KV tiles per block = ceil(c / kt_w)
+  int mb_h;     // query rows per work unit
+  int n_mb;     // work units per query block = ceil(c / mb_h)
+};
+
+// Ring order: at step s, query block i meets KV block (i - s) mod N (host i
+// receives from host i-1 and forwards to i+1).
+__host__ __device__ __forceinline__ int ring_block(int i, int s, int N) {
+  int j = i - s;
+  return j < 0 ? j + N : j;
+}
+
+// Contiguous causal: blocks j > i hold only future tokens and are skipped
+// whole.  Every other block pair is visited.
+__host__ __device__ __forceinline__ bool block_visited(const RingGeom& g, int i, int j) {
+  return !(g.causal && !g.striped && j > i);
+}
+
+// Block pairs whose mask depends on the row/column inside the block: the
+// diagonal block of a contiguous causal sweep, and every striped causal pair.
+__host__ __device__ __forceinline__ bool diag_type(const RingGeom& g, int i, int j) {
+  return g.causal && (g.striped || j == i);
+}
+
+// Inside a diag-type pair (i, j), query row rq sees key row rk iff
+// rk < rq, or rk == rq and the key token is not later than the query token:
+// contiguous j == i (same token), striped j <= i (token rk*N+j <= rq*N+i).
+// So rk is visible iff rk < rq + incl, with incl = 1 if (contiguous or j <= i).
+__host__ __device__ __forceinline__ int diag_incl(const RingGeom& g, int i, int j) {
+  return (!g.striped || j <= i) ? 1 : 0;
+}
+
+// Last KV tile of block j that a unit of query rows [r0, r0 + mb_h) needs.
+__host__ __device__ __forceinline__ int kt_last(const RingGeom& g, int i, int j, int r0) {
+  int last = g.n_kt - 1;
+  if (diag_type(g, i, j)) {
+    int d = (r0 + g.mb_h - 1) / g.kt_w;
+    if (d < last) last = d;
+  }
+  return last;
+}
+
+// Does KV tile kt of pair (i, j) need the per-element mask for rows
+// [r0, r0 + mb_h)?  Ragged last tile, or a diag-type pair whose tile reaches
+// the unit's first row.
+__host__ __device__ __forceinline__ bool tile_masked(const RingGeom& g, int i, int j, int kt, int r0) {
+  if ((kt + 1) * g.kt_w > g.c) return true;
+  return diag_type(g, i, j) && (kt * g.kt_w + g.kt_w - 1 >= r0);
+}
+
+// Exclusive upper bound on visible key rows rk for query row rq in a masked
+// tile of pair (i, j): rk visible iff rk < key_limit.
+__host__ __device__ __forceinline__ int key_limit(const RingGeom& g, int i, int j, int rq) {
+  int lim = g.c;
+  if (diag_type(g, i, j)) {
+    int d = rq + diag_incl(g, i, j);
+    if (d < lim) lim = d;
+  }
+  return lim;
+}
+
+// Number of KV tiles in the sweep of the unit (i, r0).
+__host__ __device__ __forceinline__ int unit_tiles(const RingGeom& g, int i, int r0) {
+  int T = 0;
+  for (int s = 0; s < g.N; ++s) {
+    int j = ring_block(i, s, g.N);
+    if (block_visited(g, i, j)) T += kt_last(g, i, j, r0) + 1;
+  }
+  return T;
+}
+
+// Work units are (bh, i, m): head bh, query block i, rows [m*mb_h, ...).
+// Enumeration order, per head, heaviest first (longest-processing-time) so a
+// static snake assignment balances CTAs; all units of one head are adjacent
+// so concurrently running CTAs share that head's K/V in L2.
+struct Unit {
+  int bh, i, r0;
+};
+__host__ __device__ __forceinline__ Unit unit_at(const RingGeom& g, int64_t u) {
+  const int64_t per_head = static_cast<int64_t>(g.N) * g.n_mb;
+  Unit w;
+  w.bh = static_cast<int>(u / per_head);
+  const int rem = static_cast<int>(u % per_head);
+  int i, m;
+  if (g.causal && !g.striped) {        // work grows with i, then m
+    i = g.N - 1 - rem / g.n_mb;
+    m = g.n_mb - 1 - rem % g.n_mb;
+  } else if (g.causal) {               // striped: work grows with m only
+    m = g.n_mb - 1 - rem / g.N;
+    i = rem % g.N;
+  } else {
+    i = rem / g.n_mb;
+    m = rem % g.n_mb;
+  }
+  w.i = i;
+  w.r0 = m * g.mb_h;
+  return w;
+}
+// Snake assignment: in round r CTA `cta` of `grid` takes position
+// r*grid + cta (r even) or r*grid + grid-1-cta (r odd).
+__host__ __device__ __forceinline__ int64_t snake_pos(int64_t r, int cta, int grid) {
+  return r * grid + ((r & 1) ? (grid - 1 - cta) : cta);
+}
+
+// Device status codes written on a bounded-wait time-out (first one wins).
+enum : unsigned int {
+  ST_OK = 0,
+  ST_FWD_WAIT = 0x100,  // | role/barrier id
+  ST_BWD_WAIT = 0x200,
+};
+
+// ----------------------------------------------------------- launchers
+// All return cudaError_t of the launch; arguments are validated by the caller.
+struct FwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  float* LSE;
+  int64_t B, H, S, D, N;
+  int causal, striped;
+  unsigned int* status;
+  unsigned long long* timing;  // [N*N] or null
+  cudaStream_t stream;
+  int num_sms;
+};
+cudaError_t launch_fwd_f32(const FwdArgs& a);
+cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tmap_k,
+                            const void* tmap_v);
+cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
+                         int64_t D, int bf16, cudaStream_t stream, int num_sms);
+
+struct BwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const float* LSE;
+  const void* dO;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* dq_acc;   // [B,H,S,D] float32 workspace
+  float* dvec;     // [B,H,S] float32 workspace
+  int64_t B, H, S, D, N;
+  int causal, striped;
+  unsigned int* status;
+  cudaStream_t stream;
+  int num_sms;
+};
+cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
+                            const void* tmap_v, const void* tmap_do);
+
+}  // namespace ra

@@ -1,0 +1,280 @@
+// host.cu -- the C ABI of libringattn.so (declared in include/ringattn.h):
+// argument validation, TMA tensor-map encoding, the device status word, and
+// dispatch to the kernels.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/ringattn.h"
+#include "common.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- device state
+__device__ unsigned int g_device_status;  // first bounded-wait time-out code, 0 if none
+
+constexpr int kMaxDevices = 64;
+struct DevState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;  // device address of g_device_status
+};
+DevState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(RA_ERR_UNSUPPORTED, "libringattn is built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    d.status = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return RA_OK;
+}
+
+std::atomic<uint64_t*> g_timing_buf{nullptr};
+std::atomic<size_t> g_timing_n{0};
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [BH, S, D] viewed as a 3-D tensor (D innermost); box = 64 cols x
+// `box_rows` rows x 1 head, 128-byte swizzle (one box row = 128 bytes).
+int make_map_bf16(CUtensorMap* m, const void* base, int64_t BH, int64_t S, int64_t D, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(S * D * 2)};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return RA_OK;
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_sizes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N) {
+  if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1)
+    return fail(RA_ERR_ARG, "sizes must be >= 1 (B=%lld H=%lld S=%lld D=%lld N=%lld)", (long long)B,
+                (long long)H, (long long)S, (long long)D, (long long)N);
+  if (S % N != 0) return fail(RA_ERR_ARG, "S=%lld is not a multiple of N=%lld", (long long)S, (long long)N);
+  if (B > INT_MAX / H) return fail(RA_ERR_ARG, "B*H exceeds 2^31-1");
+  if (S > INT_MAX || D > INT_MAX) return fail(RA_ERR_ARG, "S or D exceeds 2^31-1");
+  const int64_t bh = B * H;
+  if (bh > INT64_MAX / S || bh * S > INT64_MAX / D / 4) return fail(RA_ERR_ARG, "B*H*S*D overflows");
+  return RA_OK;
+}
+int check_enums(int causal, int layout, int dtype) {
+  if (causal != 0 && causal != 1) return fail(RA_ERR_ARG, "causal must be 0 or 1 (got %d)", causal);
+  if (layout != RA_CONTIGUOUS && layout != RA_STRIPED) return fail(RA_ERR_ARG, "bad layout %d", layout);
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_ARG, "bad dtype %d", dtype);
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ra_last_error(void) { return g_last_error.c_str(); }
+const char* ra_version(void) { return "ringattn 0.1 sm_103a"; }
+
+int ra_set_timing_buffer(uint64_t* dev_buf, size_t n) {
+  if (dev_buf != nullptr && n < 1) return fail(RA_ERR_ARG, "timing buffer of size 0");
+  g_timing_n.store(dev_buf ? n : 0);
+  g_timing_buf.store(dev_buf);
+  return RA_OK;
+}
+
+int ra_check_device_status(void* stream) {
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+    return fail(RA_ERR_TIMEOUT, "a device-side wait timed out (code 0x%x); outputs are unspecified", v);
+  }
+  return RA_OK;
+}
+
+int ra_fwd(const void* Q, const void* K, const void* V, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+           int causal, int layout, int dtype, void* O, float* LSE, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return fail(RA_ERR_ARG, "ra_fwd: null pointer");
+  int rc = check_sizes(B, H, S, D, N);
+  if (rc != RA_OK) return rc;
+  if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
+  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd: LSE must be 4-byte aligned");
+  if (dtype == RA_BF16) {
+    if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_fwd: bf16 path needs D == 128 (got %lld)", (long long)D);
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+      return fail(RA_ERR_ARG, "ra_fwd: bf16 tensors must be 16-byte aligned");
+  } else {
+    if (D % 4 != 0 || D > 128)
+      return fail(RA_ERR_UNSUPPORTED, "ra_fwd: f32 path needs D %% 4 == 0 and D <= 128 (got %lld)", (long long)D);
+    if (!aligned(Q, 4) || !aligned(K, 4) || !aligned(V, 4) || !aligned(O, 4))
+      return fail(RA_ERR_ARG, "ra_fwd: f32 tensors must be 4-byte aligned");
+  }
+  uint64_t* timing = g_timing_buf.load();
+  if (timing && g_timing_n.load() < static_cast<size_t>(N * N))
+    return fail(RA_ERR_ARG, "timing buffer holds %zu entries, N*N = %lld needed", g_timing_n.load(),
+                (long long)(N * N));
+  DevState* d = nullptr;
+  if ((rc = device_state(&d)) != RA_OK) return rc;
+
+  ra::FwdArgs a;
+  a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE;
+  a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
+  a.causal = causal;
+  a.striped = layout == RA_STRIPED;
+  a.status = d->status;
+  a.timing = reinterpret_cast<unsigned long long*>(timing);
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.num_sms = d->num_sms;
+  cudaError_t e;
+  if (dtype == RA_BF16) {
+    CUtensorMap mq, mk, mv;
+    if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
+    e = ra::launch_fwd_bf16(a, &mq, &mk, &mv);
+  } else {
+    e = ra::launch_fwd_f32(a);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "ra_fwd launch");
+  return RA_OK;
+}
+
+int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows, int64_t D, int dtype,
+             void* stream) {
+  if (rows < 0) return fail(RA_ERR_ARG, "ra_merge: rows < 0");
+  if (D < 1 || D > 1024) return fail(RA_ERR_ARG, "ra_merge: D must be in 1..1024 (got %lld)", (long long)D);
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_ARG, "bad dtype %d", dtype);
+  if (rows == 0) return RA_OK;
+  if (!O_a || !lse_a || !O_b || !lse_b) return fail(RA_ERR_ARG, "ra_merge: null pointer");
+  const uintptr_t oal = dtype == RA_BF16 ? 2 : 4;
+  if (!aligned(O_a, oal) || !aligned(O_b, oal) || !aligned(lse_a, 4) || !aligned(lse_b, 4))
+    return fail(RA_ERR_ARG, "ra_merge: misaligned pointer");
+  if (rows > INT64_MAX / D) return fail(RA_ERR_ARG, "ra_merge: rows*D overflows");
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  cudaError_t e = ra::launch_merge(O_a, lse_a, O_b, lse_b, rows, D, dtype == RA_BF16,
+                                   static_cast<cudaStream_t>(stream), d->num_sms);
+  if (e != cudaSuccess) return cuda_fail(e, "ra_merge launch");
+  return RA_OK;
+}
+
+size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
+  if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
+  if (B > INT_MAX / H) return 0;
+  const int64_t rows = B * H;
+  if (rows > INT64_MAX / S || rows * S > INT64_MAX / D / 8) return 0;
+  const uint64_t dq = static_cast<uint64_t>(rows * S * D) * 4;
+  const uint64_t dv = static_cast<uint64_t>(rows * S) * 4;
+  auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
+  return static_cast<size_t>(up(dq) + up(dv));
+}
+
+int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+           void* dK, void* dV, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, int causal, int layout,
+           int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!Q || !K || !V || !O || !LSE || !dO || !dQ || !dK || !dV || !workspace)
+    return fail(RA_ERR_ARG, "ra_bwd: null pointer");
+  int rc = check_sizes(B, H, S, D, N);
+  if (rc != RA_OK) return rc;
+  if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: only the bf16 path is implemented");
+  if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: bf16 path needs D == 128 (got %lld)", (long long)D);
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return fail(RA_ERR_ARG, "ra_bwd: tensors must be 16-byte aligned");
+  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_bwd: LSE must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "ra_bwd: workspace must be 256-byte aligned");
+  const size_t need = ra_bwd_workspace_bytes(B, H, S, D);
+  if (ws_bytes < need) return fail(RA_ERR_ARG, "ra_bwd: workspace of %zu bytes, %zu needed", ws_bytes, need);
+  DevState* d = nullptr;
+  if ((rc = device_state(&d)) != RA_OK) return rc;
+
+  ra::BwdArgs a;
+  a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE; a.dO = dO;
+  a.dQ = dQ; a.dK = dK; a.dV = dV;
+  const uint64_t dq_bytes = (static_cast<uint64_t>(B * H * S * D) * 4 + 255) & ~uint64_t(255);
+  a.dq_acc = static_cast<float*>(workspace);
+  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_bytes);
+  a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
+  a.causal = causal;
+  a.striped = layout == RA_STRIPED;
+  a.status = d->status;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.num_sms = d->num_sms;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
+  if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
+  if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
+  if ((rc = make_map_bf16(&mdo, dO, B * H, S, D, 128)) != RA_OK) return rc;
+  cudaError_t e = ra::launch_bwd_bf16(a, &mq, &mk, &mv, &mdo);
+  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: kernel not built");
+  if (e != cudaSuccess) return cuda_fail(e, "ra_bwd launch");
+  return RA_OK;
+}
+
+}  // extern "C"

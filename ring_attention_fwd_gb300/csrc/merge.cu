@@ -1,0 +1,107 @@
+// merge.cu -- LogSumExp merge of two partial attention states, in place.
+//
+// "Ring Attention如何让大模型突破百万Token上下文…" (answer.freetools.me),
+// section "Online Softmax": partial denominators combine as
+// l = l1 e^{m1-m} + l2 e^{m2-m}, or in log space with lse = m + ln l.  The
+// normalised outputs are re-weighted by each part's share of the total mass.
+//
+// HBM-bound elementwise kernel: each block owns whole rows, so every thread
+// reads lse_a of its row before any thread of the block overwrites it.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.cuh"
+
+namespace ra {
+namespace mrg {
+
+template <typename T, int VEC>
+struct Vec;
+template <>
+struct Vec<float, 4> {
+  using type = float4;
+};
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  using type = uint4;
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f(float v, float& x) { x = v; }
+__device__ __forceinline__ void from_f(float v, __nv_bfloat16& x) { x = __float2bfloat16_rn(v); }
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(1024) merge_kernel(T* __restrict__ Oa, float* la, const T* __restrict__ Ob,
+                                                     const float* lb, int64_t rows, int D, int cpr, int rpb) {
+  const int tid = threadIdx.x;
+  const int rsub = tid / cpr;
+  const int ch = tid % cpr;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * rpb + rsub;
+  const bool active = rsub < rpb && row < rows;
+  float A = -INFINITY, Bv = -INFINITY;
+  if (active) {
+    A = la[row];
+    Bv = lb[row];
+  }
+  __syncthreads();  // all reads of la in this block precede its writes below
+  if (!active) return;
+  const float M = fmaxf(A, Bv);
+  float wa = 0.f, wb = 0.f, lse = -INFINITY;
+  if (M != -INFINITY) {
+    const float ea = expf(A - M);
+    const float eb = expf(Bv - M);
+    const float tot = ea + eb;
+    lse = M + logf(tot);
+    wa = ea / tot;
+    wb = eb / tot;
+  }
+  const int64_t base = row * D + static_cast<int64_t>(ch) * VEC;
+  if constexpr (VEC == 1) {
+    T out;
+    from_f(wa * to_f(Oa[base]) + wb * to_f(Ob[base]), out);
+    Oa[base] = out;
+  } else {
+    using V = typename Vec<T, VEC>::type;
+    V va = *reinterpret_cast<const V*>(Oa + base);
+    V vb = *reinterpret_cast<const V*>(Ob + base);
+    T* ea = reinterpret_cast<T*>(&va);
+    const T* eb = reinterpret_cast<const T*>(&vb);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) from_f(wa * to_f(ea[k]) + wb * to_f(eb[k]), ea[k]);
+    *reinterpret_cast<V*>(Oa + base) = va;
+  }
+  if (ch == 0) la[row] = lse;
+}
+
+template <typename T, int VEC>
+cudaError_t run(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows, int64_t D,
+                cudaStream_t stream) {
+  const int cpr = static_cast<int>(D / VEC);
+  int rpb = 256 / cpr;
+  if (rpb < 1) rpb = 1;
+  const int threads = rpb * cpr;
+  const int64_t blocks = (rows + rpb - 1) / rpb;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  merge_kernel<T, VEC><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<T*>(O_a), lse_a, static_cast<const T*>(O_b), lse_b, rows, static_cast<int>(D), cpr, rpb);
+  return cudaGetLastError();
+}
+
+}  // namespace mrg
+
+cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
+                         int64_t D, int bf16, cudaStream_t stream, int /*num_sms*/) {
+  if (rows == 0) return cudaSuccess;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(O_a) | reinterpret_cast<uintptr_t>(O_b);
+  if (bf16) {
+    if (D % 8 == 0 && (al & 15) == 0) return mrg::run<__nv_bfloat16, 8>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+    return mrg::run<__nv_bfloat16, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+  }
+  if (D % 4 == 0 && (al & 15) == 0) return mrg::run<float, 4>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+  return mrg::run<float, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+}
+
+}  // namespace ra

@@ -1,0 +1,118 @@
+"""The C ABI library loads, exports every symbol ``include/ringattn.h``
+declares, and rejects bad arguments on the host before touching a GPU.
+CPU only: no call here reaches a CUDA API."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from ring_attention_fwd_gb300 import binding, build
+    if not os.path.exists(binding._LIB_PATH):
+        build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"RA_API\s+[\w\s\*]+?\b(ra_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    assert declared_symbols() == sorted([
+        "ra_fwd", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_set_timing_buffer",
+        "ra_check_device_status", "ra_last_error", "ra_version"])
+
+
+def test_library_exports_every_declared_symbol(L):
+    from ring_attention_fwd_gb300 import binding
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+        assert name in binding.SIGNATURES, name
+
+
+def test_version(L):
+    assert L.ra_version().decode().startswith("ringattn")
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(L, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, B=1, H=1, S=256, D=128, N=2, causal=1, layout=0, dtype=1, O=FAKE,
+             LSE=FAKE, stream=None)
+    a.update(kw)
+    return L.ra_fwd(a["Q"], a["K"], a["V"], a["B"], a["H"], a["S"], a["D"], a["N"], a["causal"], a["layout"],
+                    a["dtype"], a["O"], a["LSE"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(Q=None), 1, "null"),
+    (dict(LSE=None), 1, "null"),
+    (dict(S=255), 1, "multiple of N"),
+    (dict(N=0), 1, ">= 1"),
+    (dict(B=0), 1, ">= 1"),
+    (dict(causal=2), 1, "causal"),
+    (dict(layout=7), 1, "layout"),
+    (dict(dtype=9), 1, "dtype"),
+    (dict(D=64), 2, "D == 128"),
+    (dict(dtype=0, D=130), 2, "D % 4"),
+    (dict(Q=FAKE + 8), 1, "16-byte"),
+    (dict(LSE=FAKE + 2), 1, "4-byte"),
+    (dict(B=2**31, H=2), 1, "2^31"),
+    (dict(S=2**40, N=1, H=2**20), 1, "2^31-1"),
+])
+def test_fwd_rejects_bad_arguments(L, kw, code, needle):
+    assert _fwd(L, **kw) == code
+    assert needle in L.ra_last_error().decode()
+
+
+def test_merge_rejects_bad_arguments(L):
+    assert L.ra_merge(FAKE, FAKE, FAKE, FAKE, 0, 128, 1, None) == 0       # rows == 0: no-op
+    assert L.ra_merge(FAKE, FAKE, FAKE, FAKE, -1, 128, 1, None) == 1
+    assert L.ra_merge(FAKE, FAKE, FAKE, FAKE, 4, 0, 1, None) == 1
+    assert L.ra_merge(FAKE, FAKE, FAKE, FAKE, 4, 2048, 1, None) == 1
+    assert L.ra_merge(None, FAKE, FAKE, FAKE, 4, 128, 1, None) == 1
+    assert L.ra_merge(FAKE, FAKE + 2, FAKE, FAKE, 4, 128, 1, None) == 1
+    assert L.ra_merge(FAKE, FAKE, FAKE, FAKE, 4, 128, 5, None) == 1
+
+
+def test_bwd_workspace_size(L):
+    B, H, S, D = 1, 32, 65536, 128
+    up = lambda x: (x + 255) // 256 * 256
+    assert L.ra_bwd_workspace_bytes(B, H, S, D) == up(B * H * S * D * 4) + up(B * H * S * 4)
+    assert L.ra_bwd_workspace_bytes(1, 1, 3, 128) == up(3 * 128 * 4) + up(12)
+    assert L.ra_bwd_workspace_bytes(0, 1, 1, 1) == 0
+
+
+def test_bwd_rejects_bad_arguments(L):
+    def call(**kw):
+        a = dict(B=1, H=1, S=256, D=128, N=2, causal=1, layout=1, dtype=1, ws=FAKE, ws_bytes=1 << 30)
+        a.update(kw)
+        return L.ra_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["S"], a["D"],
+                        a["N"], a["causal"], a["layout"], a["dtype"], a["ws"], a["ws_bytes"], None)
+    assert call(ws=None) == 1
+    assert call(S=100, N=3) == 1
+    assert call(dtype=0) == 2
+    assert call(D=64) == 2
+    assert call(ws_bytes=16) == 1 and "workspace" in L.ra_last_error().decode()
+    assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
+
+
+def test_timing_buffer_arguments(L):
+    assert L.ra_set_timing_buffer(FAKE, 0) == 1
+    assert L.ra_set_timing_buffer(None, 0) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from ring_attention_fwd_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no non-CUDA fallback"):
+        binding.lib()

@@ -1,0 +1,126 @@
+"""Forward parity: CUDA path (through the C ABI) vs the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import TOL, fwd_full_check, fwd_sampled_check, workload_inputs
+from ring_attention_fwd_gb300.inputs import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ra():
+    import ring_attention_fwd_gb300 as ra
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return ra
+
+
+def test_tiny_f32_workload(ra):
+    w = WORKLOADS["tiny_f32"]
+    eo, el = fwd_full_check(ra, workload_inputs(w), w["N"], w["causal"], w["layout"], "f32")
+    assert eo <= TOL["f32"]["o"] and el <= TOL["f32"]["lse"], (eo, el)
+
+
+@pytest.mark.parametrize("B,H,S,D,N,causal,layout", [
+    (1, 1, 256, 64, 4, True, "contiguous"),
+    (1, 2, 300, 32, 3, True, "striped"),        # c = 100: ragged tiles
+    (2, 1, 192, 128, 1, False, "contiguous"),
+    (1, 1, 130, 8, 5, True, "striped"),          # c = 26
+])
+def test_f32_shapes(ra, B, H, S, D, N, causal, layout):
+    inp = make_inputs(B, H, S, D, seed=100 + S, dtype="f32")
+    eo, el = fwd_full_check(ra, inp, N, causal, layout, "f32")
+    assert eo <= TOL["f32"]["o"] and el <= TOL["f32"]["lse"], (eo, el)
+
+
+BF16_CASES = [
+    (1, 1, 256, 1, True, "contiguous"),     # one block
+    (1, 2, 512, 2, True, "contiguous"),
+    (1, 2, 512, 2, True, "striped"),
+    (2, 1, 1024, 4, False, "contiguous"),
+    (1, 1, 384, 3, True, "striped"),        # c = 128: unit taller than a block
+    (1, 2, 600, 3, True, "contiguous"),     # c = 200: ragged KV tile and unit
+    (1, 1, 1000, 5, True, "striped"),       # c = 200, striped
+    (1, 1, 128, 8, True, "striped"),        # c = 16: every tile ragged
+    (1, 3, 2048, 4, True, "striped"),
+    (1, 2, 4096, 8, False, "striped"),
+    (3, 2, 1536, 6, True, "contiguous"),    # c = 256
+]
+
+
+@pytest.mark.parametrize("B,H,S,N,causal,layout", BF16_CASES)
+def test_bf16_shapes(ra, B, H, S, N, causal, layout):
+    inp = make_inputs(B, H, S, 128, seed=200 + S + N, dtype="bf16")
+    eo, el = fwd_full_check(ra, inp, N, causal, layout, "bf16")
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+
+
+def test_bf16_deterministic(ra):
+    inp = {k: v.cuda() for k, v in make_inputs(1, 4, 2048, 128, seed=7).items()}
+    o1, l1 = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
+    o2, l2 = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_causal_8k_workload_full(ra):
+    w = WORKLOADS["causal_8k"]
+    eo, el = fwd_full_check(ra, workload_inputs(w), w["N"], w["causal"], w["layout"], "bf16")
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+
+
+@pytest.mark.parametrize("layout", ["striped", "contiguous"])
+def test_balance_32k_workload_sampled(ra, layout):
+    w = WORKLOADS["balance_32k"]
+    inp = workload_inputs(w)
+    eo, el, _, _ = fwd_sampled_check(ra, inp, w["N"], w["causal"], layout, [(0, 0), (0, 9), (0, 15)], 256, 3)
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+
+
+def test_long_128k_workload_sampled(ra):
+    """The 131072-token workload, in the launch configuration the benchmark
+    times; sampled rows of three heads against the oracle.  The call must not
+    allocate device memory beyond its outputs (working set of the method:
+    a constant number of blocks per virtual host, here none extra)."""
+    w = WORKLOADS["long_128k"]
+    inp = workload_inputs(w)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    B, H, S, D = inp["q"].shape
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    ra.fwd(dev["q"], dev["k"], dev["v"], w["N"], True, "contiguous", o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.cuda.max_memory_allocated() == base
+    del dev, o, lse
+    eo, el, _, _ = fwd_sampled_check(ra, inp, w["N"], w["causal"], w["layout"], [(0, 0), (0, 17), (0, 31)],
+                                     256, 4)
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+
+
+def test_fwdbwd_64k_workload_forward_sampled(ra):
+    w = WORKLOADS["fwdbwd_64k"]
+    inp = workload_inputs(w)
+    eo, el, _, _ = fwd_sampled_check(ra, inp, w["N"], w["causal"], w["layout"], [(0, 0), (0, 31)], 256, 5)
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+
+
+def test_per_device_timing_buffer(ra):
+    """Timing hooks: every visited (virtual host, ring step) gets time, every
+    skipped one (contiguous causal, j > i) none."""
+    N = 4
+    inp = {k: v.cuda() for k, v in make_inputs(1, 2, 2048, 128, seed=9).items()}
+    buf = torch.zeros(N * N, dtype=torch.int64, device="cuda")
+    ra.set_timing_buffer(buf)
+    try:
+        ra.fwd(inp["q"], inp["k"], inp["v"], N, True, "contiguous")
+        torch.cuda.synchronize()
+    finally:
+        ra.set_timing_buffer(None)
+    t = buf.view(N, N).cpu().numpy()
+    for i in range(N):
+        for s in range(N):
+            j = (i - s) % N
+            assert (t[i, s] > 0) == (j <= i), (i, s, t)
