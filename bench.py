@@ -1,0 +1,361 @@
+"""Benchmark: ring-order blockwise attention forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k]
+
+A step is one pass of the whole path over one batch of synthetic input: the
+forward (O, LSE) followed by the backward (dQ, dK, dV) from the saved state.
+Default workload: 131072 tokens, 32 heads of dim 128, 32 ring blocks of
+4096, causal, contiguous, inputs N(0,1) x 0.5 in bf16.  The inputs (1 GiB
+each) are larger than L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas; the real multi-GPU ring exchange is not built), the
+timing is the max over ranks and `value` sums the ranks' work.
+
+`--impl reference` times the CPU oracle (float64 NumPy) on the host cores, on
+a bounded sample of the same workload, and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-order blockwise attn fwd+bwd TFLOP/s, % GB300 BF16 peak (S=128K)"
+UNIT = "TFLOP/s"
+
+# DRAM traffic per launch of the dominant kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# source it was taken on: the hash of csrc/<file> at capture time.
+NCU_TRAFFIC = {
+    # "fwd_bf16.cu": {"sha256": "...", "workload": "long_128k", "bytes_per_launch": ...},
+}
+
+
+def _src_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "ring_attention_fwd_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows if len(r) > 8 for k in range(4)
+                          if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(inp, w, budget_s: float):
+    """Time the oracle on sampled query rows of one head (forward LSE/O and
+    the dQ rows of the backward), growing the sample until `budget_s` is
+    spent.  Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle as orc
+    q = inp["q"][0, 0].double().numpy()
+    k = inp["k"][0, 0].double().numpy()
+    v = inp["v"][0, 0].double().numpy()
+    do = inp["do"][0, 0].double().numpy() if "do" in inp else v
+    S, D, N = w["S"], w["D"], w["N"]
+    pos = orc.token_positions(S, N, w["layout"])
+    rng = np.random.default_rng(0)
+    flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        rows = np.sort(rng.choice(S, size=64, replace=False))
+        orc.attention_rows(q, k, v, rows, N, w["causal"], w["layout"])
+        orc.attention_bwd_dq_rows(q, k, v, do, rows, N, w["causal"], w["layout"])
+        vis = (pos[rows] + 1) if w["causal"] else np.full(rows.size, S)
+        # forward 4*D per visible pair; the backward's dQ rows 2.5x that (convention)
+        flops += float(vis.sum()) * 4 * D * 3.5
+        rows_done += rows.size
+    dt = time.perf_counter() - t0
+    return flops, dt, f"{rows_done} random query rows of head 0 (forward O/LSE + backward dQ), row by row"
+
+
+def run_reference(args, w):
+    import torch
+    from ring_attention_fwd_gb300.inputs import make_inputs
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    inp = make_inputs(1, 1, w["S"], w["D"], w["seed"], dtype=w["dtype"], scale=w["scale"], with_grad=True)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(inp, w, per_step / 4)
+    tot_f = tot_t = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, t, desc = oracle_sample(inp, w, per_step)
+        tot_f += f
+        tot_t += t
+    val = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: w[k] for k in ("B", "H", "S", "D", "N", "causal", "layout")}},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}; numpy float64, BLAS threads = {cores}"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, w):
+    import torch
+    import ring_attention_fwd_gb300 as ra
+    from ring_attention_fwd_gb300 import flops as fl
+    from ring_attention_fwd_gb300.inputs import make_inputs
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    B, H, S, D, N = w["B"], w["H"], w["S"], w["D"], w["N"]
+    causal, layout = w["causal"], w["layout"]
+    inp = make_inputs(B, H, S, D, w["seed"], dtype=w["dtype"], scale=w["scale"], with_grad=True)
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    dev = {k: v.cuda() for k, v in host.items()}
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
+    wsb = ra.bwd_workspace_bytes(B, H, S, D)
+    work = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def has_bwd():
+        try:
+            ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, causal, layout, dq=dq, dk=dk, dv=dv,
+                   workspace=work)
+            return True
+        except ra.RingAttnError as e:
+            if e.code == ra.binding.RA_ERR_UNSUPPORTED:
+                return False
+            raise
+
+    ra.fwd(dev["q"], dev["k"], dev["v"], N, causal, layout, o=o, lse=lse)
+    with_bwd = has_bwd()
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    f_fwd = fl.fwd_flops(B, H, S, D, causal)
+    f_bwd = fl.bwd_flops(B, H, S, D, causal) if with_bwd else 0
+    f_step = f_fwd + f_bwd
+
+    ev = []
+
+    def step(record):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ra.fwd(dev["q"], dev["k"], dev["v"], N, causal, layout, o=o, lse=lse)
+        e1.record(stream)
+        if with_bwd:
+            ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, causal, layout, dq=dq, dk=dk, dv=dv,
+                   workspace=work)
+        e2.record(stream)
+        if record:
+            ev.append((e0, e1, e2))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ra.check_device_status()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        total_ms = float(tt.item())
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev) if with_bwd else None
+    ms_step = total_ms / args.steps
+    value = f_step * ws / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, compute, D2H of every output
+    outs_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                 "lse": torch.empty_like(lse, device="cpu").pin_memory()}
+    if with_bwd:
+        for n in ("dq", "dk", "dv"):
+            outs_host[n] = torch.empty_like(dq, device="cpu").pin_memory()
+    in_names = ["q", "k", "v"] + (["do"] if with_bwd else [])
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+
+    def e2e_step():
+        for n in in_names:
+            dev[n].copy_(host[n], non_blocking=True)
+        ra.fwd(dev["q"], dev["k"], dev["v"], N, causal, layout, o=o, lse=lse)
+        if with_bwd:
+            ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, causal, layout, dq=dq, dk=dk, dv=dv,
+                   workspace=work)
+        outs_host["o"].copy_(o, non_blocking=True)
+        outs_host["lse"].copy_(lse, non_blocking=True)
+        if with_bwd:
+            outs_host["dq"].copy_(dq, non_blocking=True)
+            outs_host["dk"].copy_(dk, non_blocking=True)
+            outs_host["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 3))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    burst, sustained, src = _peaks()
+    dom_is_bwd = with_bwd and bwd_ms is not None and bwd_ms > fwd_ms
+    dom_ms = bwd_ms if dom_is_bwd else fwd_ms
+    dom_flops = f_bwd if dom_is_bwd else f_fwd
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    src_file = "bwd_bf16.cu" if dom_is_bwd else "fwd_bf16.cu"
+    tr = NCU_TRAFFIC.get(src_file)
+    traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash(src_file) and \
+        tr["workload"] == args.workload else None
+    roofline = {"bound": "tensor", "kernel": "bwd" if dom_is_bwd else "fwd", "achieved": achieved,
+                "peak": sustained, "unit": UNIT, "frac": achieved / sustained, "traffic": traffic,
+                "peak_kind": f"{src} sustained bf16 (burst {burst})", "frac_of_burst": achieved / burst}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "S": S, "D": D, "N": N, "causal": causal,
+                   "layout": layout, "input_scale": w["scale"], "step": "fwd+bwd" if with_bwd else "fwd only",
+                   "l2": "inputs larger than L2 (1 GiB per tensor), no flush",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "fwd": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                "frac_of_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / sustained},
+        "bwd": ({"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                 "frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / sustained} if with_bwd else None),
+        "tokens_per_s": B * S * ws / (ms_step * 1e-3),
+        "roofline": roofline,
+        "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + (3 if with_bwd else 0)),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = len(os.sched_getaffinity(0))
+        inp1 = {k: v[:1, :1] for k, v in inp.items()}
+        f, t, desc = oracle_sample(inp1, w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc + f"; {t:.1f} s of numpy float64"}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_128k")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from ring_attention_fwd_gb300.inputs import WORKLOADS
+    w = dict(WORKLOADS[args.workload])
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
