@@ -188,7 +188,7 @@ def run_ours(args, w):
     o = torch.empty_like(dev["q"])
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
     dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
-    wsb = ra.bwd_workspace_bytes(B, H, S, D)
+    wsb = ra.bwd_workspace_bytes(B, H, S, D, N)
     work = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 

@@ -106,10 +106,12 @@ RA_API int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b
 
 /*
  * ra_bwd_workspace_bytes -- size of the caller-allocated workspace ra_bwd
- * needs for these sizes (float32 dQ accumulator [B,H,S,D] and the per-row
- * D_vec = rowsum(dO * O) [B,H,S], each 256-byte aligned).  0 on bad sizes.
+ * needs for these sizes: a float32 dQ accumulator [B,H,S,D], and per query
+ * row D_vec = rowsum(dO * O) and LSE * log2(e), each stored per 128-row query
+ * tile of every block ([B,H,N,ceil(S/N/128),128] float32).  Each part starts
+ * 256-byte aligned.  Returns 0 on bad sizes (as ra_bwd would reject them).
  */
-RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
+RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N);
 
 /*
  * ra_bwd -- backward pass from the saved output and LSE.
@@ -124,8 +126,9 @@ RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D)
  *
  *   Q, K, V, O, dO : [B,H,S,D] inputs;  LSE [B,H,S] float32 input (as ra_fwd
  *   wrote it).  dQ, dK, dV : [B,H,S,D] outputs of `dtype`.  16-byte aligned.
- *   workspace : device memory of at least ra_bwd_workspace_bytes(...) bytes,
- *   256-byte aligned; its contents on entry do not matter.
+ *   workspace : device memory of at least ra_bwd_workspace_bytes(B,H,S,D,N)
+ *   bytes, 256-byte aligned; its contents on entry do not matter.  Calls that
+ *   share a workspace must not overlap on the GPU.
  *   Sizes, causal, layout as for ra_fwd; RA_BF16 with D == 128 only.
  * Errors: RA_ERR_ARG (also: workspace too small), RA_ERR_UNSUPPORTED,
  * RA_ERR_CUDA.

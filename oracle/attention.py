@@ -297,6 +297,41 @@ def attention_bwd_dq_rows(q, k, v, do, rows, n_blocks: int, causal: bool, layout
     return (dS @ k) / np.sqrt(D)
 
 
+def attention_bwd_kv_rows(q, k, v, do, key_rows, n_blocks: int, causal: bool, layout: str,
+                          row_chunk: int = 512):
+    """dK and dV of selected key rows of ONE head, from Q, K, V, dO alone.
+
+    Every query row that can see one of the keys (all rows, or under the causal
+    rule the rows whose token is not earlier than the earliest selected key) has
+    its O and LSE recomputed from the definition (``attention_rows``); then
+        dV(k) = sum_q P(q,k) dO(q),   dS(q,k) = P(q,k) (dO(q).v_k - D_vec(q)),
+        dK(k) = sum_q dS(q,k) q / sqrt(D),   D_vec(q) = dO(q).O(q).
+    Returns (dK [len(key_rows), D], dV [len(key_rows), D]).
+    """
+    S, D = q.shape
+    key_rows = np.asarray(key_rows, dtype=np.int64)
+    pos = token_positions(S, n_blocks, layout)
+    if causal:
+        q_rows = np.nonzero(pos >= pos[key_rows].min())[0]
+    else:
+        q_rows = np.arange(S)
+    dK = np.zeros((key_rows.size, D))
+    dV = np.zeros((key_rows.size, D))
+    kk, vk = k[key_rows], v[key_rows]
+    for c0 in range(0, q_rows.size, row_chunk):
+        rows = q_rows[c0:c0 + row_chunk]
+        o_r, lse_r = attention_rows(q, k, v, rows, n_blocks, causal, layout)
+        s = (q[rows] @ kk.T) / np.sqrt(D)
+        vis = visible(pos[rows], pos[key_rows], causal) & np.isfinite(lse_r)[:, None]
+        P = np.where(vis, np.exp(np.where(vis, s - lse_r[:, None], -np.inf)), 0.0)
+        dP = do[rows] @ vk.T
+        Dvec = (do[rows] * o_r).sum(axis=1)
+        dS = P * (dP - Dvec[:, None])
+        dV += P.T @ do[rows]
+        dK += (dS.T @ q[rows]) / np.sqrt(D)
+    return dK, dV
+
+
 # ----------------------------------------------------------------------------
 # Work per virtual device (load balance)
 # ----------------------------------------------------------------------------

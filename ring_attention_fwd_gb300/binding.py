@@ -28,7 +28,7 @@ _i64, _vp, _fp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ct
 SIGNATURES = {
     "ra_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp, _vp]),
     "ra_merge": (_int, [_vp, _fp, _vp, _fp, _i64, _i64, _int, _vp]),
-    "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                       _int, _int, _int, _vp, _sz, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
@@ -119,8 +119,8 @@ def merge(o_a, lse_a, o_b, lse_b, *, stream=None):
     return o_a, lse_a
 
 
-def bwd_workspace_bytes(B, H, S, D) -> int:
-    return int(lib().ra_bwd_workspace_bytes(B, H, S, D))
+def bwd_workspace_bytes(B, H, S, D, N) -> int:
+    return int(lib().ra_bwd_workspace_bytes(B, H, S, D, N))
 
 
 def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
@@ -133,7 +133,7 @@ def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = bwd_workspace_bytes(B, H, S, D)
+    need = bwd_workspace_bytes(B, H, S, D, int(n_blocks))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(lib().ra_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),

@@ -159,7 +159,8 @@ struct BwdArgs {
   void* dK;
   void* dV;
   float* dq_acc;   // [B,H,S,D] float32 workspace
-  float* dvec;     // [B,H,S] float32 workspace
+  float* lse2;     // [B,H,N,ceil(c/128),128] float32 workspace: LSE * log2(e)
+  float* dvec;     // same layout: rowsum(dO * O)
   int64_t B, H, S, D, N;
   int causal, striped;
   unsigned int* status;

@@ -223,15 +223,34 @@ int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64
   return RA_OK;
 }
 
-size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
-  if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
-  if (B > INT_MAX / H) return 0;
-  const int64_t rows = B * H;
-  if (rows > INT64_MAX / S || rows * S > INT64_MAX / D / 8) return 0;
-  const uint64_t dq = static_cast<uint64_t>(rows * S * D) * 4;
-  const uint64_t dv = static_cast<uint64_t>(rows * S) * 4;
+}  // extern "C"
+
+namespace {
+// Workspace parts: dQ accumulator, then lse2 and D_vec per padded query row.
+struct WsLayout {
+  uint64_t dq_bytes, vec_bytes, total;
+};
+bool ws_layout(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, WsLayout* w) {
+  if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1 || S % N != 0) return false;
+  if (B > INT_MAX / H) return false;
+  const int64_t bh = B * H;
+  if (bh > INT64_MAX / S || bh * S > INT64_MAX / D / 8) return false;
+  const int64_t c = S / N;
+  const int64_t padded = N * ((c + 127) / 128) * 128;   // per head
+  if (bh > INT64_MAX / padded / 8) return false;
   auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
-  return static_cast<size_t>(up(dq) + up(dv));
+  w->dq_bytes = up(static_cast<uint64_t>(bh * S * D) * 4);
+  w->vec_bytes = up(static_cast<uint64_t>(bh * padded) * 4);
+  w->total = w->dq_bytes + 2 * w->vec_bytes;
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N) {
+  WsLayout w;
+  return ws_layout(B, H, S, D, N, &w) ? static_cast<size_t>(w.total) : 0;
 }
 
 int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
@@ -249,17 +268,19 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
     if (!aligned(p, 16)) return fail(RA_ERR_ARG, "ra_bwd: tensors must be 16-byte aligned");
   if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_bwd: LSE must be 4-byte aligned");
   if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "ra_bwd: workspace must be 256-byte aligned");
-  const size_t need = ra_bwd_workspace_bytes(B, H, S, D);
-  if (ws_bytes < need) return fail(RA_ERR_ARG, "ra_bwd: workspace of %zu bytes, %zu needed", ws_bytes, need);
+  WsLayout wl;
+  if (!ws_layout(B, H, S, D, N, &wl)) return fail(RA_ERR_ARG, "ra_bwd: workspace size overflows");
+  if (ws_bytes < wl.total)
+    return fail(RA_ERR_ARG, "ra_bwd: workspace of %zu bytes, %llu needed", ws_bytes, (unsigned long long)wl.total);
   DevState* d = nullptr;
   if ((rc = device_state(&d)) != RA_OK) return rc;
 
   ra::BwdArgs a;
   a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE; a.dO = dO;
   a.dQ = dQ; a.dK = dK; a.dV = dV;
-  const uint64_t dq_bytes = (static_cast<uint64_t>(B * H * S * D) * 4 + 255) & ~uint64_t(255);
   a.dq_acc = static_cast<float*>(workspace);
-  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_bytes);
+  a.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.dq_bytes);
+  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.dq_bytes + wl.vec_bytes);
   a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
   a.causal = causal;
   a.striped = layout == RA_STRIPED;

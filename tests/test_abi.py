@@ -84,11 +84,14 @@ def test_merge_rejects_bad_arguments(L):
 
 
 def test_bwd_workspace_size(L):
-    B, H, S, D = 1, 32, 65536, 128
     up = lambda x: (x + 255) // 256 * 256
-    assert L.ra_bwd_workspace_bytes(B, H, S, D) == up(B * H * S * D * 4) + up(B * H * S * 4)
-    assert L.ra_bwd_workspace_bytes(1, 1, 3, 128) == up(3 * 128 * 4) + up(12)
-    assert L.ra_bwd_workspace_bytes(0, 1, 1, 1) == 0
+    B, H, S, D, N = 1, 32, 65536, 128, 16
+    padded = N * ((S // N + 127) // 128) * 128
+    assert L.ra_bwd_workspace_bytes(B, H, S, D, N) == up(B * H * S * D * 4) + 2 * up(B * H * padded * 4)
+    # ragged blocks: 3 blocks of 200 rows -> 2 query tiles of 128 each per block
+    assert L.ra_bwd_workspace_bytes(1, 2, 600, 128, 3) == up(2 * 600 * 128 * 4) + 2 * up(2 * 3 * 256 * 4)
+    assert L.ra_bwd_workspace_bytes(0, 1, 1, 1, 1) == 0
+    assert L.ra_bwd_workspace_bytes(1, 1, 10, 128, 3) == 0      # S % N != 0
 
 
 def test_bwd_rejects_bad_arguments(L):

@@ -1,0 +1,144 @@
+"""Backward parity: CUDA ra_bwd (through the C ABI) vs the CPU oracle.
+
+Tolerance for dQ, dK, dV (bf16 inputs, float32 accumulation, bf16 outputs):
+max |g - ref| <= 2e-2 * max(1, max |ref|), and relative Frobenius error
+<= 1e-2.  Derivation: P and dS enter the tensor cores rounded to bf16
+(relative 2^-9); the outputs are rounded to bf16 (relative 2^-9); float32
+accumulation adds ~1e-6 relative; so ~4e-3 of the largest gradient entry,
+with a 5x margin for sums of correlated rounding errors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from gpu_helpers import max_err, sample_rows, workload_inputs
+from ring_attention_fwd_gb300.inputs import WORKLOADS, as_float64, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ra():
+    import ring_attention_fwd_gb300 as ra
+    assert torch.cuda.is_available()
+    return ra
+
+
+def _close(g, ref, name):
+    g = np.asarray(g, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = max(1.0, float(np.abs(ref).max()))
+    e = max_err(g, ref)
+    assert e <= 2e-2 * scale, f"{name}: max err {e:.3e} (scale {scale:.3e})"
+    fro = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
+    assert fro <= 1e-2, f"{name}: relative Frobenius {fro:.3e}"
+
+
+BWD_CASES = [
+    (1, 1, 256, 1, True, "contiguous"),
+    (1, 2, 512, 2, True, "contiguous"),
+    (1, 2, 512, 2, True, "striped"),
+    (2, 1, 1024, 4, False, "contiguous"),
+    (1, 1, 384, 3, True, "striped"),
+    (1, 2, 600, 3, True, "contiguous"),     # c = 200: ragged KV and query tiles
+    (1, 1, 1000, 5, True, "striped"),       # c = 200, striped
+    (1, 1, 128, 8, True, "striped"),        # c = 16
+    (1, 3, 2048, 4, True, "striped"),
+    (1, 2, 2048, 8, False, "striped"),
+]
+
+
+@pytest.mark.parametrize("B,H,S,N,causal,layout", BWD_CASES)
+def test_bwd_shapes_from_oracle_state(ra, B, H, S, N, causal, layout):
+    """The kernel alone: it is given the oracle's O (rounded to bf16) and LSE
+    (rounded to float32); the expected gradient uses those same rounded values."""
+    inp = make_inputs(B, H, S, 128, seed=300 + S + N, with_grad=True)
+    q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
+    o_ref, lse_ref = orc.naive_attention(q, k, v, N, causal, layout)
+    o_bf = torch.from_numpy(o_ref).to(torch.bfloat16)
+    lse_f = torch.from_numpy(lse_ref).float()
+    rq, rk, rv = orc.attention_bwd(q, k, v, o_bf.double().numpy(), lse_f.double().numpy(), do, N, causal, layout)
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
+    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o_bf.cuda(), lse_f.cuda(), dev["do"], N, causal, layout)
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    _close(dq.double().cpu().numpy(), rq, "dQ")
+    _close(dk.double().cpu().numpy(), rk, "dK")
+    _close(dv.double().cpu().numpy(), rv, "dV")
+
+
+@pytest.mark.parametrize("layout", ["striped", "contiguous"])
+def test_fwd_then_bwd_against_exact_gradient(ra, layout):
+    """The composition: the GPU forward's (O, LSE) feed the GPU backward; the
+    oracle computes the gradient from Q, K, V, dO alone."""
+    B, H, S, N = 1, 2, 1536, 6
+    inp = make_inputs(B, H, S, 128, seed=401, with_grad=True)
+    q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
+    o_ref, lse_ref = orc.naive_attention(q, k, v, N, True, layout)
+    rq, rk, rv = orc.attention_bwd(q, k, v, o_ref, lse_ref, do, N, True, layout)
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
+    o, lse = ra.fwd(dev["q"], dev["k"], dev["v"], N, True, layout)
+    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, True, layout)
+    torch.cuda.synchronize()
+    _close(dq.double().cpu().numpy(), rq, "dQ")
+    _close(dk.double().cpu().numpy(), rk, "dK")
+    _close(dv.double().cpu().numpy(), rv, "dV")
+
+
+def test_bwd_deterministic_dk_dv_and_workspace_reuse(ra):
+    """dK and dV are written by one CTA each (bit-identical across runs); dQ
+    accumulates with float atomics, so only closeness is required.  A
+    workspace reused without clearing gives the same result."""
+    inp = {k: v.cuda() for k, v in make_inputs(1, 2, 1024, 128, seed=5, with_grad=True).items()}
+    o, lse = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
+    ws = torch.full((ra.bwd_workspace_bytes(1, 2, 1024, 128, 4),), 0x7f, dtype=torch.uint8, device="cuda")
+    a = ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped", workspace=ws)
+    b = ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped", workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert float((a[0].float() - b[0].float()).abs().max()) <= 1e-2
+
+
+def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only):
+    inp = workload_inputs(w)
+    N, causal, layout = w["N"], w["causal"], w["layout"]
+    B, H, S, D = inp["q"].shape
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
+    o, lse = ra.fwd(dev["q"], dev["k"], dev["v"], N, causal, layout)
+    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, causal, layout)
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t.float()).all())
+    del o, lse, dev
+    for h in dq_heads:
+        rows = sample_rows(S, N, 96, 7 + h)
+        q, k, v, do = (inp[x][0, h].to(torch.float64).numpy() for x in ("q", "k", "v", "do"))
+        ref = orc.attention_bwd_dq_rows(q, k, v, do, rows, N, causal, layout)
+        _close(dq[0, h, torch.from_numpy(rows).cuda()].double().cpu().numpy(), ref, f"dQ rows head {h}")
+    q, k, v, do = (inp[x][0, kv_head].to(torch.float64).numpy() for x in ("q", "k", "v", "do"))
+    pos = orc.token_positions(S, N, layout)
+    rng = np.random.default_rng(11)
+    if late_only:   # keys among the last 2048 tokens: only ~2048 queries see them
+        cand = np.nonzero(pos >= S - 2048)[0]
+    else:
+        cand = np.arange(S)
+    keys = np.sort(rng.choice(cand, size=n_keys, replace=False))
+    rk, rv = orc.attention_bwd_kv_rows(q, k, v, do, keys, N, causal, layout)
+    kidx = torch.from_numpy(keys).cuda()
+    _close(dk[0, kv_head, kidx].double().cpu().numpy(), rk, "dK rows")
+    _close(dv[0, kv_head, kidx].double().cpu().numpy(), rv, "dV rows")
+
+
+def test_fwdbwd_64k_workload_sampled(ra):
+    """The 65536-token striped forward+backward workload at full size: dQ on
+    sampled query rows of two heads, dK/dV on random key rows of one head
+    (every query of that head recomputed by the oracle)."""
+    _sampled_bwd_check(ra, WORKLOADS["fwdbwd_64k"], dq_heads=(0, 31), kv_head=5, n_keys=24, late_only=False)
+
+
+def test_long_128k_workload_backward_sampled(ra):
+    """The benchmark's workload and launch configuration: dQ on sampled rows of
+    two heads, dK/dV on key rows among the last 2048 tokens of one head."""
+    _sampled_bwd_check(ra, WORKLOADS["long_128k"], dq_heads=(0, 20), kv_head=9, n_keys=64, late_only=True)

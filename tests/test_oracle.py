@@ -326,6 +326,20 @@ def test_dq_rows_match_full_backward():
                                    dq[rows], atol=1e-13)
 
 
+def test_kv_rows_match_full_backward():
+    rng = np.random.default_rng(20)
+    S, N, D = 48, 4, 8
+    q, k, v, do = (_rand(rng, S, D) for _ in range(4))
+    for layout in LAYOUTS:
+        for causal in (True, False):
+            o, lse = orc.attention_rows(q, k, v, np.arange(S), N, causal, layout)
+            _, dk, dv = orc.attention_bwd_head(q, k, v, o, lse, do, N, causal, layout)
+            keys = np.array([0, 5, 12, 30, 47])
+            gk, gv = orc.attention_bwd_kv_rows(q, k, v, do, keys, N, causal, layout, row_chunk=7)
+            np.testing.assert_allclose(gk, dk[keys], atol=1e-13)
+            np.testing.assert_allclose(gv, dv[keys], atol=1e-13)
+
+
 # ------------------------------------------------------------- work per device
 def test_visible_pairs_brute_force_and_balance():
     for S, N in ((16, 4), (64, 8), (96, 3)):
