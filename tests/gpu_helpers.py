@@ -77,6 +77,8 @@ def fwd_sampled_check(ra, inp: dict, N: int, causal: bool, layout: str, heads, n
     return eo, el, o, lse
 
 
-def workload_inputs(w: dict) -> dict:
+def workload_inputs(w: dict, with_grad: bool = False) -> dict:
+    """The workload's seeded inputs; dO is drawn after Q, K, V, so asking for it
+    leaves Q, K, V unchanged."""
     return make_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], dtype=w["dtype"], scale=w["scale"],
-                       with_grad=w["grad"])
+                       with_grad=w["grad"] or with_grad)

@@ -101,7 +101,7 @@ def test_bwd_deterministic_dk_dv_and_workspace_reuse(ra):
 
 
 def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only):
-    inp = workload_inputs(w)
+    inp = workload_inputs(w, with_grad=True)
     N, causal, layout = w["N"], w["causal"], w["layout"]
     B, H, S, D = inp["q"].shape
     dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
