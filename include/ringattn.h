@@ -141,6 +141,36 @@ RA_API int ra_bwd(const void* Q, const void* K, const void* V, const void* O,
            void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * ra_bwd_noalloc -- ra_bwd for callers that cannot allocate device memory.
+ *
+ * No passage of the pages corresponds to this entry point: it exists for
+ * callers that cannot hand ra_bwd a workspace, e.g. code running inside a host
+ * framework that owns all device memory through its own pool and forbids side
+ * allocations, or a latency-critical path that must not call cudaMalloc
+ * (which can synchronise the device).  It computes exactly what ra_bwd
+ * computes, with the same arguments minus the workspace, and allocates
+ * nothing: the workspace is a fixed 48 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ *   Arguments, results and errors as for ra_bwd.  Sizes whose
+ *   ra_bwd_workspace_bytes(B,H,S,D,N) exceeds 48 MiB (50331648 bytes) are
+ *   rejected with RA_ERR_ARG and a message saying so; e.g. B*H*S up to about
+ *   90,000 rows at D = 128 fit.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array and leave their intermediate values in it;
+ *   every value a call reads is first written by that same call.  Calls whose
+ *   executions overlap on the GPU (different streams, or different host
+ *   threads, on the same device) race on the array and give wrong results:
+ *   serialise them.
+ */
+RA_API int ra_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+           const float* LSE, const void* dO,
+           void* dQ, void* dK, void* dV,
+           int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+           int causal, int layout, int dtype, void* stream);
+
+/*
  * ra_set_timing_buffer -- per-virtual-host time accounting for later bf16
  * ra_fwd calls from any thread (process-wide setting; NULL disables).
  * `dev_buf` is a caller-owned device array of n uint64 that the caller zeroes;

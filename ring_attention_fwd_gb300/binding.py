@@ -31,6 +31,8 @@ SIGNATURES = {
     "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                       _int, _int, _int, _vp, _sz, _vp]),
+    "ra_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                              _int, _int, _int, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
     "ra_last_error": (ctypes.c_char_p, []),
@@ -140,6 +142,27 @@ def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "
                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, int(n_blocks),
                         int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], workspace.data_ptr(),
                         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
+                dq=None, dk=None, dv=None, stream=None):
+    """Backward without a workspace argument, for callers that cannot allocate
+    device memory: the library uses its own fixed 48 MiB device array (larger
+    problems raise RingAttnError).  The output tensors may be passed in, so a
+    caller that cannot allocate can reuse its own buffers.  Concurrent calls on
+    one device race on that array.  Returns (dq, dk, dv)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _need(t, name, q.dtype)
+    _need(lse, "lse", torch.float32)
+    B, H, S, D = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().ra_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D,
+                                int(n_blocks), int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype],
+                                _stream_ptr(stream)))
     return dq, dk, dv
 
 

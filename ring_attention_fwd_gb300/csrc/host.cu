@@ -126,6 +126,11 @@ int check_enums(int causal, int layout, int dtype) {
 
 }  // namespace
 
+namespace ra {
+// Lets other translation units of the library report through ra_last_error().
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace ra
+
 extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }

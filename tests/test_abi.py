@@ -26,7 +26,7 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
-        "ra_fwd", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_set_timing_buffer",
+        "ra_fwd", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
         "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
@@ -106,6 +106,14 @@ def test_bwd_rejects_bad_arguments(L):
     assert call(D=64) == 2
     assert call(ws_bytes=16) == 1 and "workspace" in L.ra_last_error().decode()
     assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
+
+
+def test_bwd_noalloc_rejects_sizes_before_touching_a_gpu(L):
+    def call(B, H, S, N):
+        return L.ra_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, S, 128, N, 1, 0, 1,
+                                None)
+    assert call(1, 1, 100, 3) == 1 and "invalid sizes" in L.ra_last_error().decode()
+    assert call(1, 32, 65536, 16) == 1 and "more than the fixed" in L.ra_last_error().decode()
 
 
 def test_timing_buffer_arguments(L):
