@@ -106,10 +106,11 @@ RA_API int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b
 
 /*
  * ra_bwd_workspace_bytes -- size of the caller-allocated workspace ra_bwd
- * needs for these sizes: a float32 dQ accumulator [B,H,S,D], and per query
- * row D_vec = rowsum(dO * O) and LSE * log2(e), each stored per 128-row query
- * tile of every block ([B,H,N,ceil(S/N/128),128] float32).  Each part starts
- * 256-byte aligned.  Returns 0 on bad sizes (as ra_bwd would reject them).
+ * needs for these sizes: per query row D_vec = rowsum(dO * O) and
+ * LSE * log2(e), each stored per 128-row query tile of every block
+ * ([B,H,N,ceil(S/N/128),128] float32, 8 bytes per padded row in all), each
+ * part 256-byte aligned.  Returns 0 on bad sizes (as ra_bwd would reject
+ * them).
  */
 RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N);
 
@@ -122,7 +123,10 @@ RA_API size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D,
  *     P = exp(Q K^T / sqrt(D) - LSE) on visible entries (0 elsewhere),
  *     dV = P^T dO,  dP = dO V^T,  D_vec = rowsum(dO * O),
  *     dS = P * (dP - D_vec),  dQ = dS K / sqrt(D),  dK = dS^T Q / sqrt(D).
- * Each KV tile sweeps the query blocks that see it in ring order.
+ * Each KV tile sweeps the query blocks that see it in ring order (dK, dV);
+ * each query tile sweeps the KV blocks in the forward's ring order (dQ).
+ * No atomics: every output element is written once, so results are
+ * bit-reproducible.
  *
  *   Q, K, V, O, dO : [B,H,S,D] inputs;  LSE [B,H,S] float32 input (as ra_fwd
  *   wrote it).  dQ, dK, dV : [B,H,S,D] outputs of `dtype`.  16-byte aligned.
@@ -154,8 +158,8 @@ RA_API int ra_bwd(const void* Q, const void* K, const void* V, const void* O,
  *
  *   Arguments, results and errors as for ra_bwd.  Sizes whose
  *   ra_bwd_workspace_bytes(B,H,S,D,N) exceeds 48 MiB (50331648 bytes) are
- *   rejected with RA_ERR_ARG and a message saying so; e.g. B*H*S up to about
- *   90,000 rows at D = 128 fit.
+ *   rejected with RA_ERR_ARG and a message saying so; about 6 million query
+ *   rows B*H*S fit (e.g. 32 heads of 131072 tokens need 32 MiB).
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   All calls share the one array and leave their intermediate values in it;

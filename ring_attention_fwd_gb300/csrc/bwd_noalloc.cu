@@ -23,8 +23,8 @@ void set_last_error(const std::string& msg);  // host.cu: the message ra_last_er
 
 namespace {
 
-// Largest workspace ra_bwd_noalloc can serve: 48 MiB, e.g. B*H = 8 heads of
-// 8192 rows at head dim 128 (32 MiB of dQ accumulator plus the two vectors).
+// Largest workspace ra_bwd_noalloc can serve: 48 MiB, 8 bytes per query row
+// (padded to 128-row tiles per block): about 6 million rows B*H*S.
 constexpr size_t kScratchBytes = size_t(48) << 20;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 

@@ -158,7 +158,6 @@ struct BwdArgs {
   void* dQ;
   void* dK;
   void* dV;
-  float* dq_acc;   // [B,H,S,D] float32 workspace
   float* lse2;     // [B,H,N,ceil(c/128),128] float32 workspace: LSE * log2(e)
   float* dvec;     // same layout: rowsum(dO * O)
   int64_t B, H, S, D, N;

@@ -231,9 +231,9 @@ int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64
 }  // extern "C"
 
 namespace {
-// Workspace parts: dQ accumulator, then lse2 and D_vec per padded query row.
+// Workspace parts: lse2 and D_vec per padded query row.
 struct WsLayout {
-  uint64_t dq_bytes, vec_bytes, total;
+  uint64_t vec_bytes, total;
 };
 bool ws_layout(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, WsLayout* w) {
   if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1 || S % N != 0) return false;
@@ -244,9 +244,8 @@ bool ws_layout(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, WsLayout* 
   const int64_t padded = N * ((c + 127) / 128) * 128;   // per head
   if (bh > INT64_MAX / padded / 8) return false;
   auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
-  w->dq_bytes = up(static_cast<uint64_t>(bh * S * D) * 4);
   w->vec_bytes = up(static_cast<uint64_t>(bh * padded) * 4);
-  w->total = w->dq_bytes + 2 * w->vec_bytes;
+  w->total = 2 * w->vec_bytes;
   return true;
 }
 }  // namespace
@@ -283,9 +282,8 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
   ra::BwdArgs a;
   a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE; a.dO = dO;
   a.dQ = dQ; a.dK = dK; a.dV = dV;
-  a.dq_acc = static_cast<float*>(workspace);
-  a.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.dq_bytes);
-  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.dq_bytes + wl.vec_bytes);
+  a.lse2 = static_cast<float*>(workspace);
+  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.vec_bytes);
   a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
   a.causal = causal;
   a.striped = layout == RA_STRIPED;

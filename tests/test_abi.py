@@ -87,9 +87,9 @@ def test_bwd_workspace_size(L):
     up = lambda x: (x + 255) // 256 * 256
     B, H, S, D, N = 1, 32, 65536, 128, 16
     padded = N * ((S // N + 127) // 128) * 128
-    assert L.ra_bwd_workspace_bytes(B, H, S, D, N) == up(B * H * S * D * 4) + 2 * up(B * H * padded * 4)
+    assert L.ra_bwd_workspace_bytes(B, H, S, D, N) == 2 * up(B * H * padded * 4)
     # ragged blocks: 3 blocks of 200 rows -> 2 query tiles of 128 each per block
-    assert L.ra_bwd_workspace_bytes(1, 2, 600, 128, 3) == up(2 * 600 * 128 * 4) + 2 * up(2 * 3 * 256 * 4)
+    assert L.ra_bwd_workspace_bytes(1, 2, 600, 128, 3) == 2 * up(2 * 3 * 256 * 4)
     assert L.ra_bwd_workspace_bytes(0, 1, 1, 1, 1) == 0
     assert L.ra_bwd_workspace_bytes(1, 1, 10, 128, 3) == 0      # S % N != 0
 
@@ -113,7 +113,7 @@ def test_bwd_noalloc_rejects_sizes_before_touching_a_gpu(L):
         return L.ra_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, H, S, 128, N, 1, 0, 1,
                                 None)
     assert call(1, 1, 100, 3) == 1 and "invalid sizes" in L.ra_last_error().decode()
-    assert call(1, 32, 65536, 16) == 1 and "more than the fixed" in L.ra_last_error().decode()
+    assert call(1, 64, 131072, 32) == 1 and "more than the fixed" in L.ra_last_error().decode()
 
 
 def test_timing_buffer_arguments(L):

@@ -54,7 +54,7 @@ def test_no_alloc_backward_matches_workspace_backward():
 
 def test_no_alloc_backward_rejects_too_large():
     import ring_attention_fwd_gb300 as ra
-    x = torch.empty((1, 32, 65536, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((1, 32, 65536), dtype=torch.float32, device="cuda")
+    x = torch.empty((1, 64, 131072, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 64, 131072), dtype=torch.float32, device="cuda")
     with pytest.raises(ra.RingAttnError, match="more than the fixed"):
-        ra.bwd_noalloc(x, x, x, x, lse, x, 16, True, "striped", dq=x, dk=x, dv=x)
+        ra.bwd_noalloc(x, x, x, x, lse, x, 32, True, "contiguous", dq=x, dk=x, dv=x)
