@@ -14,19 +14,26 @@
 //                   query tile (rows past a block's end get D_vec = 0 and
 //                   +inf, so they drop out of P by themselves).
 //   2. dkv_kernel   KV-stationary.  A work unit is one 128-row KV tile of one
-//                   head; dK and dV accumulate in TMEM while the query tiles
-//                   of blocks i = j, j+1, ... (mod N) that see KV block j --
-//                   the hosts block j travels to around the ring -- stream
-//                   past.  Per query tile: S^T = K Q^T, dP^T = V dO^T;
-//                   P^T and dS^T (bf16) are written back over S^T and dP^T in
-//                   TMEM; dV += P^T dO and dK += dS^T Q read them from there.
+//                   head, held in shared memory, with dK and dV accumulating
+//                   in TMEM while the query tiles of blocks i = j, j+1, ...
+//                   (mod N) that see KV block j -- the hosts block j travels
+//                   to around the ring -- stream past.  Per query tile:
+//                   S^T = K Q^T, dP^T = V dO^T; P^T and dS^T (bf16) are packed
+//                   over dP^T in TMEM; dV += P^T dO and dK += dS^T Q read them
+//                   from there.
 //   3. dq_kernel    Query-stationary, visiting KV tiles in the forward's ring
-//                   order.  Per KV tile: S = Q K^T, dP = dO V^T; dS (bf16)
-//                   over S in TMEM; dQ += dS K with dQ accumulating in TMEM.
+//                   order; Q and dO sit in TMEM as A operands.  Per KV tile:
+//                   S = Q K^T, dP = dO V^T; dS (bf16) packed over dP in TMEM;
+//                   dQ += dS K with dQ accumulating in TMEM.
+// Every MMA is 128 wide (an MMA instruction costs ~93 clocks at any size on
+// this part, so wide ones keep the tensor pipe fed).  Overlap: the elementwise
+// warps release S as soon as it is in registers, so the next tile's S MMA runs
+// while they compute; P^T/dS^T go over dP, whose next write follows the MMAs
+// that read them.
 // Both main kernels: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
-// TMEM owner, warps 4-7 and 8-11 the two halves (64 columns each) of the
-// elementwise work, one thread per TMEM lane (row); each half writes only the
-// TMEM columns it read.
+// TMEM owner, warps 4-7 and 8-11 the elementwise work, one thread per TMEM lane
+// (row); warpgroup g owns columns [64g, 64g+64) and writes its packed bf16
+// results only over columns it has read.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -41,22 +48,23 @@ namespace bwd {
 constexpr int BT = 128;        // rows per KV tile and per query tile
 constexpr int HD = 128;
 constexpr int THREADS = 384;
-constexpr int NSTAGE = 2;
 constexpr uint32_t TILE_BYTES = BT * HD * 2;  // 32 KB
 constexpr uint32_t BOX_BYTES = TILE_BYTES / 2;
 constexpr uint32_t VEC_BYTES = BT * 4;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
-// Packed bf16 column of the 16-wide K-slice kk of a 128-column operand that
-// the two halves wrote at columns [0,32) and [64,96) of a region.
-__device__ __forceinline__ uint32_t half_packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
 
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {   // K-major operand, K-slice kk
-  return sdesc(tile + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024, SWZ_128B);
+// Descriptors of a 128B-swizzled tile (two 64-column boxes): the K-slice kk
+// (16 elements) of a K-major operand, or of an MN-major operand, as offsets
+// from the tile's kk = 0 descriptor.
+__device__ __forceinline__ uint64_t kdesc0(uint32_t tile) { return sdesc(tile, 16, 1024, SWZ_128B); }
+__device__ __forceinline__ uint64_t mndesc0(uint32_t tile) { return sdesc(tile, BOX_BYTES, 1024, SWZ_128B); }
+__device__ __forceinline__ uint64_t kslice(uint64_t d0, int kk) {
+  return sdesc_add(d0, (kk >> 2) * BOX_BYTES + (kk & 3) * 32);
 }
-__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {  // MN-major operand, K-slice kk
-  return sdesc(tile + kk * 16 * 128, BOX_BYTES, 1024, SWZ_128B);
-}
+__device__ __forceinline__ uint64_t mnslice(uint64_t d0, int kk) { return sdesc_add(d0, kk * 16 * 128); }
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) { return kslice(kdesc0(tile), kk); }
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) { return mnslice(mndesc0(tile), kk); }
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -101,20 +109,41 @@ __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int
   return ((static_cast<int64_t>(bh) * g.N + i) * g.n_mb + qt) * BT;
 }
 
+// Copies one 128-element bf16 row from global memory into 64 TMEM columns of
+// this thread's lane (element pairs packed low-first, the layout of a K-major
+// A operand), or zeros when the row lies past the end of the tensor.
+__device__ __forceinline__ void row_to_tmem(const __nv_bfloat16* src, uint32_t tcol, bool in_bounds) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t v[32];
+    const uint4* s4 = reinterpret_cast<const uint4*>(src) + half * 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 x = in_bounds ? __ldg(s4 + k) : make_uint4(0u, 0u, 0u, 0u);
+      v[4 * k] = x.x;
+      v[4 * k + 1] = x.y;
+      v[4 * k + 2] = x.z;
+      v[4 * k + 3] = x.w;
+    }
+    tmem_st32(tcol + half * 32, v);
+  }
+}
+
 // ============================================================== dK, dV
 namespace kv {
+constexpr int QSTAGE = 2;
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
-constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;             // NSTAGE tiles
-constexpr uint32_t OFF_DO = OFF_Q + NSTAGE * TILE_BYTES;   // NSTAGE tiles
-constexpr uint32_t OFF_VEC = OFF_DO + NSTAGE * TILE_BYTES; // NSTAGE x (lse2[128], dvec[128])
-constexpr uint32_t OFF_BAR = OFF_VEC + NSTAGE * 2 * VEC_BYTES;
+constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;              // QSTAGE tiles
+constexpr uint32_t OFF_DO = OFF_Q + QSTAGE * TILE_BYTES;    // QSTAGE tiles
+constexpr uint32_t OFF_VEC = OFF_DO + QSTAGE * TILE_BYTES;  // QSTAGE x (lse2[128], dvec[128])
+constexpr uint32_t OFF_BAR = OFF_VEC + QSTAGE * 2 * VEC_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
 
 struct Bars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[NSTAGE], q_empty[NSTAGE];
-  uint64_t s_full, p_full, dkv_full, dkv_empty, drain;
+  uint64_t q_full[QSTAGE], q_empty[QSTAGE];
+  uint64_t s_full, s_free, p_full, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -149,6 +178,11 @@ __device__ __forceinline__ int unit_steps(const RingGeom& g, int j, int kt) {
   }
   return T;
 }
+// Packed bf16 columns of the 16-query K-slice kk of P^T / dS^T inside the dP^T
+// region: warpgroup g (queries [64g, 64g+64)) packs P^T at [64g, 64g+32) and
+// dS^T at [64g+32, 64g+64).
+__device__ __forceinline__ uint32_t pcol_p(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
+__device__ __forceinline__ uint32_t pcol_ds(int kk) { return 64 * (kk >> 2) + 32 + 8 * (kk & 3); }
 
 __global__ void __launch_bounds__(THREADS, 1)
 dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -166,11 +200,12 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < QSTAGE; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 256);
@@ -186,6 +221,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // TMEM: dV [0,128) dK [128,256) S^T [256,384) dP^T [384,512); P^T and dS^T
+  // are packed (bf16) over dP^T once it has been read.
   const uint32_t T_DV = tmem, T_DK = tmem + 128, T_S = tmem + 256, T_DP = tmem + 384;
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int grid = gridDim.x, cta = blockIdx.x;
@@ -219,8 +256,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const int i = (j + s) % g.N;
           if (!q_block_visited(g, i, j)) continue;
           for (int qt = qt_first(g, i, j, kt); qt < g.n_mb; ++qt, ++it) {
-            const int st = it % NSTAGE;
-            if (!(ok = mbar_wait(&bars->q_empty[st], ((it / NSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 2))) break;
+            const int st = it % QSTAGE;
+            if (!(ok = mbar_wait(&bars->q_empty[st], ((it / QSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 2))) break;
             mbar_arrive_expect_tx(&bars->q_full[st], 2 * TILE_BYTES + 2 * VEC_BYTES);
             const int qrow = i * g.c + qt * BT;
             for (int h = 0; h < 2; ++h) {
@@ -235,19 +272,29 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
       }
       if (!ok) {
-        for (uint32_t k = (it > NSTAGE ? it - NSTAGE : 0); k < it; ++k)
-          mbar_drain(&bars->q_full[k % NSTAGE], (k / NSTAGE) & 1, 200000000ull);
+        for (uint32_t k = (it > QSTAGE ? it - QSTAGE : 0); k < it; ++k)
+          mbar_drain(&bars->q_full[k % QSTAGE], (k / QSTAGE) & 1, 200000000ull);
         if (nkv > 0) mbar_drain(&bars->kv_full, (nkv - 1) & 1, 200000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A, B K-major
+      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A, B K-major, N = 128
       constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A from TMEM, B MN-major
-      const uint32_t sK = sbase + OFF_K, sV = sbase + OFF_V;
-      uint32_t it = 0, kv_ph = 0, pf_ph = 0, dkve_ph = 0;
-      bool ok = true, first_unit = true;
+      const uint64_t dK0 = kdesc0(sbase + OFF_K), dV0 = kdesc0(sbase + OFF_V);
+      uint32_t it = 0, kv_ph = 0, sf_ph = 0, pf_ph = 0, dkve_ph = 0;
+      bool ok = true, first_unit = true, first_s = true;
+      auto issue_s = [=](int st) {   // S^T = K Q^T
+        const uint64_t bq = kdesc0(sbase + OFF_Q + st * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_S, kslice(dK0, kk), kslice(bq, kk), ID_KK, kk > 0);
+      };
+      auto issue_dp = [=](int st) {  // dP^T = V dO^T
+        const uint64_t bdo = kdesc0(sbase + OFF_DO + st * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kslice(dV0, kk), kslice(bdo, kk), ID_KK, kk > 0);
+      };
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
@@ -256,17 +303,26 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const int T = unit_steps(g, j, kt);
         if (!(ok = mbar_wait(&bars->kv_full, kv_ph, wc, ST_BWD_WAIT | 3))) break;
         kv_ph ^= 1;
+        if (!(ok = mbar_wait(&bars->q_full[it % QSTAGE], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 4))) break;
+        if (!first_s) {   // S^T region: the previous tile's S^T must have been read
+          if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
+          sf_ph ^= 1;
+        }
+        first_s = false;
+        tc_fence_after();
+        issue_s(it % QSTAGE);
+        issue_dp(it % QSTAGE);   // dP^T region: last read by the previous tile's dV / dK MMAs
+        mma_commit(&bars->s_full);
         for (int t = 0; t < T && ok; ++t, ++it) {
-          const int st = it % NSTAGE;
-          const uint32_t sQ = sbase + OFF_Q + st * TILE_BYTES, sDO = sbase + OFF_DO + st * TILE_BYTES;
-          if (!(ok = mbar_wait(&bars->q_full[st], (it / NSTAGE) & 1, wc, ST_BWD_WAIT | 4))) break;
-          tc_fence_after();
-          // S^T and dP^T overwrite the P^T / dS^T the previous dV / dK MMAs read: issued after them.
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_S, kdesc(sK, kk), kdesc(sQ, kk), ID_KK, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kdesc(sV, kk), kdesc(sDO, kk), ID_KK, kk > 0);
-          mma_commit(&bars->s_full);
+          const int st = it % QSTAGE;
+          const int nst = (it + 1) % QSTAGE;
+          if (t + 1 < T) {   // next tile's S^T as soon as this tile's S^T is in registers
+            if (!(ok = mbar_wait(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
+            if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
+            sf_ph ^= 1;
+            tc_fence_after();
+            issue_s(nst);
+          }
           if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 5))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
@@ -275,13 +331,18 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           }
           tc_fence_after();
           const uint32_t acc = t > 0 ? 1u : 0u;
+          const uint64_t mdo = mndesc0(sbase + OFF_DO + st * TILE_BYTES), mq = mndesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO
-            mma_ts(T_DV, T_S + half_packed_col(kk), mndesc(sDO, kk), ID_TM, (kk > 0) | acc);
+            mma_ts(T_DV, T_DP + pcol_p(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q
-            mma_ts(T_DK, T_DP + half_packed_col(kk), mndesc(sQ, kk), ID_TM, (kk > 0) | acc);
+            mma_ts(T_DK, T_DP + pcol_ds(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
           mma_commit(&bars->q_empty[st]);
+          if (t + 1 < T) {
+            issue_dp(nst);
+            mma_commit(&bars->s_full);
+          }
         }
         if (!ok) break;
         mma_commit(&bars->kv_empty);
@@ -292,8 +353,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else if (warp >= 4) {
-    // -------------------------------------- P^T, dS^T (one half of the columns)
-    const int half = (warp - 4) >> 2;                    // query columns [64*half, 64*half + 64)
+    // ------------------------------------------------ P^T and dS^T, epilogue
+    const int grp = (warp - 4) >> 2;                     // query columns [64*grp, +64)
     const int quad = warp & 3;
     const int t_row = quad * 32 + lane;                  // key row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -305,53 +366,60 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       if (u >= p.num_units) break;
       int bh, j, kt;
       unit_at(g, u, bh, j, kt);
-      const bool key_ok = kt * BT + t_row < g.c;
+      const int lk = kt * BT + t_row;                    // key row inside block j
+      const bool key_ok = lk < g.c;
       for (int s = 0; s < g.N && ok; ++s) {
         const int i = (j + s) % g.N;
         if (!q_block_visited(g, i, j)) continue;
         const bool dpair = diag_type(g, i, j);
         const int incl = diag_incl(g, i, j);
         for (int qt = qt_first(g, i, j, kt); qt < g.n_mb && ok; ++qt, ++it) {
-          const int st = it % NSTAGE;
-          if (!(ok = mbar_wait(&bars->q_full[st], (it / NSTAGE) & 1, wc, ST_BWD_WAIT | 7))) break;
+          const int st = it % QSTAGE;
+          if (!(ok = mbar_wait(&bars->q_full[st], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 7))) break;
           if (!(ok = mbar_wait(&bars->s_full, s_ph, wc, ST_BWD_WAIT | 8))) break;
           s_ph ^= 1;
           tc_fence_after();
-          // query column q is visible to this key row iff q >= vis_lo
+          const uint32_t tS = T_S + lane_off + 64 * grp;
+          const uint32_t tDP = T_DP + lane_off + 64 * grp;
+          uint32_t sv[64], dpv[64];
+          tmem_ld32(tS, sv);
+          tmem_ld32(tS + 32, sv + 32);
+          tmem_ld32(tDP, dpv);
+          tmem_ld32(tDP + 32, dpv + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);
+          // query column q of the tile is visible to this key row iff q >= vis_lo
           int vis_lo = 0;
           if (!key_ok) vis_lo = BT;
           else if (dpair && qt == kt) vis_lo = t_row + 1 - incl;
-          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_VEC + st * 2 * VEC_BYTES);
+          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_VEC + st * 2 * VEC_BYTES) + 64 * grp;
           const float* dvec = lse2 + BT;
+          const int q0 = 64 * grp;
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            const int c0 = half * 64 + ch * 32;
-            uint32_t sv[32], dpv[32];
-            tmem_ld32(T_S + lane_off + c0, sv);
-            tmem_ld32(T_DP + lane_off + c0, dpv);
-            tmem_ld_wait();
+          for (int hh = 0; hh < 2; ++hh) {
             uint32_t pk[16], dk[16];
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + k);
-              const float4 d4 = *reinterpret_cast<const float4*>(dvec + c0 + k);
-              float p0 = hw_exp2(fmaf(__uint_as_float(sv[k]), sl2, -l4.x));
-              float p1 = hw_exp2(fmaf(__uint_as_float(sv[k + 1]), sl2, -l4.y));
-              float p2 = hw_exp2(fmaf(__uint_as_float(sv[k + 2]), sl2, -l4.z));
-              float p3 = hw_exp2(fmaf(__uint_as_float(sv[k + 3]), sl2, -l4.w));
-              if (c0 + k < vis_lo) p0 = 0.f;
-              if (c0 + k + 1 < vis_lo) p1 = 0.f;
-              if (c0 + k + 2 < vis_lo) p2 = 0.f;
-              if (c0 + k + 3 < vis_lo) p3 = 0.f;
+              const int c = hh * 32 + k;
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+              const float4 d4 = *reinterpret_cast<const float4*>(dvec + c);
+              float p0 = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+              float p1 = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+              float p2 = hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+              float p3 = hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+              if (q0 + c < vis_lo) p0 = 0.f;
+              if (q0 + c + 1 < vis_lo) p1 = 0.f;
+              if (q0 + c + 2 < vis_lo) p2 = 0.f;
+              if (q0 + c + 3 < vis_lo) p3 = 0.f;
               pk[k >> 1] = pack_bf16x2(p0, p1);
               pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
-              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[k]) - d4.x), p1 * (__uint_as_float(dpv[k + 1]) - d4.y));
+              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[c]) - d4.x), p1 * (__uint_as_float(dpv[c + 1]) - d4.y));
               dk[(k >> 1) + 1] =
-                  pack_bf16x2(p2 * (__uint_as_float(dpv[k + 2]) - d4.z), p3 * (__uint_as_float(dpv[k + 3]) - d4.w));
+                  pack_bf16x2(p2 * (__uint_as_float(dpv[c + 2]) - d4.z), p3 * (__uint_as_float(dpv[c + 3]) - d4.w));
             }
-            // packed bf16 over this half's own columns: [0,32) or [64,96)
-            tmem_st16(T_S + lane_off + half * 64 + ch * 16, pk);
-            tmem_st16(T_DP + lane_off + half * 64 + ch * 16, dk);
+            tmem_st16(tDP + hh * 16, pk);        // P^T over this group's own dP^T columns
+            tmem_st16(tDP + 32 + hh * 16, dk);   // dS^T
           }
           tmem_st_wait();
           tc_fence_before();
@@ -359,12 +427,12 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
       }
       if (!ok) break;
-      // ---- epilogue: half 0 writes dV, half 1 writes dK / sqrt(d)
+      // ---- epilogue: group 0 writes dV, group 1 writes dK / sqrt(d)
       if (!(ok = mbar_wait(&bars->dkv_full, dkv_ph, wc, ST_BWD_WAIT | 9))) break;
       dkv_ph ^= 1;
       tc_fence_after();
-      const int64_t krow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(j) * g.c + kt * BT + t_row;
-      if (half == 0)
+      const int64_t krow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(j) * g.c + lk;
+      if (grp == 0)
         store_row_bf16(T_DV + lane_off, p.dV + krow * HD, 1.f, key_ok, HD);
       else
         store_row_bf16(T_DK + lane_off, p.dK + krow * HD, p.inv_sqrt_d, key_ok, HD);
@@ -384,24 +452,25 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
 // ============================================================== dQ
 namespace q {
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_DO = OFF_Q + TILE_BYTES;
-constexpr uint32_t OFF_K = OFF_DO + TILE_BYTES;            // NSTAGE tiles
-constexpr uint32_t OFF_V = OFF_K + NSTAGE * TILE_BYTES;    // NSTAGE tiles
-constexpr uint32_t OFF_BAR = OFF_V + NSTAGE * TILE_BYTES;
+constexpr int KSTAGE = 3;
+constexpr uint32_t OFF_K = 0;                               // KSTAGE tiles
+constexpr uint32_t OFF_V = OFF_K + KSTAGE * TILE_BYTES;     // KSTAGE tiles
+constexpr uint32_t OFF_BAR = OFF_V + KSTAGE * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
 
 struct Bars {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[NSTAGE], v_full[NSTAGE], kv_empty[NSTAGE];
-  uint64_t s_full, p_full, dq_full, dq_empty, drain;
+  uint64_t k_full[KSTAGE], v_full[KSTAGE], kv_empty[KSTAGE];
+  uint64_t qo_full, qo_empty, s_full, s_free, p_full, dq_full, dq_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
+// Packed bf16 column of the 16-key K-slice kk of dS inside the dP region:
+// warpgroup g (keys [64g, 64g+64)) packs its dS at [64g, 64g+32).
+__device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
 
 __global__ void __launch_bounds__(THREADS, 1)
-dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const Params p) {
+dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+          const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ dO, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const uint32_t sbase = smem_u32(smem);
@@ -413,14 +482,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     return;
   }
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < KSTAGE; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
+    mbar_init(&bars->qo_full, 256);
+    mbar_init(&bars->qo_empty, 1);
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 256);
@@ -436,41 +506,30 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t T_DQ = tmem, T_S = tmem + 128, T_DP = tmem + 256;
+  // TMEM: dQ [0,128) Q [128,192) dO [192,256) (bf16 rows, A operands)
+  //       S [256,384) dP [384,512); dS is packed (bf16) over dP once read.
+  const uint32_t T_DQ = tmem, T_Q = tmem + 128, T_DO = tmem + 192, T_S = tmem + 256, T_DP = tmem + 384;
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int grid = gridDim.x, cta = blockIdx.x;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      uint32_t it = 0, nq = 0, qe_ph = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
-        if (nq > 0) {
-          if (!(ok = mbar_wait(&bars->q_empty, qe_ph, wc, ST_BWD_WAIT | 0x11))) break;
-          qe_ph ^= 1;
-        }
-        mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
-        const int qrow = w.i * g.c + w.r0;
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(smem + OFF_Q + h * BOX_BYTES, &tmQ, &bars->q_full, h * 64, qrow, w.bh);
-          tma_load_3d(smem + OFF_DO + h * BOX_BYTES, &tmDO, &bars->q_full, h * 64, qrow, w.bh);
-        }
-        ++nq;
         for (int s = 0; s < g.N && ok; ++s) {
           const int j = ring_block(w.i, s, g.N);
           if (!block_visited(g, w.i, j)) continue;
           const int last = kt_last(g, w.i, j, w.r0);
           for (int kt = 0; kt <= last; ++kt, ++it) {
-            const int st = it % NSTAGE;
-            if (!(ok = mbar_wait(&bars->kv_empty[st], ((it / NSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x12))) break;
+            const int st = it % KSTAGE;
+            if (!(ok = mbar_wait(&bars->kv_empty[st], ((it / KSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x12))) break;
             const int krow = j * g.c + kt * BT;
             mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
@@ -481,42 +540,63 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
           }
         }
       }
-      if (!ok) {
-        for (uint32_t k = (it > NSTAGE ? it - NSTAGE : 0); k < it; ++k) {
-          mbar_drain(&bars->k_full[k % NSTAGE], (k / NSTAGE) & 1, 200000000ull);
-          mbar_drain(&bars->v_full[k % NSTAGE], (k / NSTAGE) & 1, 200000000ull);
+      if (!ok)
+        for (uint32_t k = (it > KSTAGE ? it - KSTAGE : 0); k < it; ++k) {
+          mbar_drain(&bars->k_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
+          mbar_drain(&bars->v_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
         }
-        if (nq > 0) mbar_drain(&bars->q_full, (nq - 1) & 1, 200000000ull);
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);
-      constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);
-      const uint32_t sQ = sbase + OFF_Q, sDO = sbase + OFF_DO;
-      uint32_t it = 0, q_ph = 0, pf_ph = 0, dqe_ph = 0;
-      bool ok = true, first_unit = true;
+      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A (TMEM), B K-major, N = 128
+      constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A (TMEM), B MN-major
+      uint32_t it = 0, qo_ph = 0, sf_ph = 0, pf_ph = 0, dqe_ph = 0;
+      bool ok = true, first_unit = true, first_s = true;
+      auto issue_s = [=](int st) {   // S = Q K^T
+        const uint64_t bk = kdesc0(sbase + OFF_K + st * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ts(T_S, T_Q + kk * 8, kslice(bk, kk), ID_KK, kk > 0);
+      };
+      auto issue_dp = [=](int st) {  // dP = dO V^T
+        const uint64_t bv = kdesc0(sbase + OFF_V + st * TILE_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ts(T_DP, T_DO + kk * 8, kslice(bv, kk), ID_KK, kk > 0);
+      };
+      auto wait_kv = [&](uint32_t k_it) -> bool {
+        const int st = k_it % KSTAGE;
+        const uint32_t ph = (k_it / KSTAGE) & 1;
+        if (!mbar_wait(&bars->k_full[st], ph, wc, ST_BWD_WAIT | 0x14)) return false;
+        if (!mbar_wait(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15)) return false;
+        return true;
+      };
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
         const int T = unit_tiles(g, w.i, w.r0);
-        if (!(ok = mbar_wait(&bars->q_full, q_ph, wc, ST_BWD_WAIT | 0x13))) break;
-        q_ph ^= 1;
+        if (!(ok = mbar_wait(&bars->qo_full, qo_ph, wc, ST_BWD_WAIT | 0x13))) break;
+        qo_ph ^= 1;
+        if (!(ok = wait_kv(it))) break;
+        if (!first_s) {   // S region: the previous tile's S must have been read
+          if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c))) break;
+          sf_ph ^= 1;
+        }
+        first_s = false;
+        tc_fence_after();
+        issue_s(it % KSTAGE);
+        issue_dp(it % KSTAGE);   // dP region: last read by the previous tile's dQ MMAs
+        mma_commit(&bars->s_full);
         for (int t = 0; t < T && ok; ++t, ++it) {
-          const int st = it % NSTAGE;
-          const uint32_t ph = (it / NSTAGE) & 1;
-          const uint32_t sK = sbase + OFF_K + st * TILE_BYTES, sV = sbase + OFF_V + st * TILE_BYTES;
-          if (!(ok = mbar_wait(&bars->k_full[st], ph, wc, ST_BWD_WAIT | 0x14))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_S, kdesc(sQ, kk), kdesc(sK, kk), ID_KK, kk > 0);
-          if (!(ok = mbar_wait(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kdesc(sDO, kk), kdesc(sV, kk), ID_KK, kk > 0);
-          mma_commit(&bars->s_full);
+          const int st = it % KSTAGE;
+          const int nst = (it + 1) % KSTAGE;
+          if (t + 1 < T) {   // next tile's S as soon as this tile's S is in registers
+            if (!(ok = wait_kv(it + 1))) break;
+            if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c))) break;
+            sf_ph ^= 1;
+            tc_fence_after();
+            issue_s(nst);
+          }
           if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 0x16))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
@@ -524,12 +604,16 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             dqe_ph ^= 1;
           }
           tc_fence_after();
+          const uint64_t mk = mndesc0(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS from TMEM, K MN-major)
-            mma_ts(T_DQ, T_S + half_packed_col(kk), mndesc(sK, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
+          for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS packed in TMEM, K MN-major)
+            mma_ts(T_DQ, T_DP + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
           mma_commit(&bars->kv_empty[st]);
-          if (t == T - 1) {
-            mma_commit(&bars->q_empty);
+          if (t + 1 < T) {
+            issue_dp(nst);
+            mma_commit(&bars->s_full);
+          } else {
+            mma_commit(&bars->qo_empty);
             mma_commit(&bars->dq_full);
           }
         }
@@ -539,19 +623,31 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else if (warp >= 4) {
-    // -------------------------------------- dS (one half of the key columns)
-    const int half = (warp - 4) >> 2;                    // key columns [64*half, 64*half + 64)
+    // ----------------------------------------- Q/dO rows, dS, epilogue
+    const int grp = (warp - 4) >> 2;                     // key columns [64*grp, +64)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                    // query row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t s_ph = 0, dq_ph = 0;
-    bool ok = true;
+    uint32_t s_ph = 0, dq_ph = 0, qoe_ph = 0;
+    bool ok = true, first_unit = true;
     for (int64_t r = 0; ok; ++r) {
       const int64_t u = snake_pos(r, cta, grid);
       if (u >= p.num_units) break;
       const Unit w = unit_at(g, u);
       const int rq = w.r0 + row;
+      const int64_t grow = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
+      // ---- this unit's Q (group 0) or dO (group 1) row into TMEM
+      if (!first_unit) {
+        if (!(ok = mbar_wait(&bars->qo_empty, qoe_ph, wc, ST_BWD_WAIT | 0x1b))) break;
+        qoe_ph ^= 1;
+        tc_fence_after();
+      }
+      first_unit = false;
+      row_to_tmem((grp == 0 ? Q : dO) + grow * HD, (grp == 0 ? T_Q : T_DO) + lane_off, w.i * g.c + rq < p.S);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->qo_full);
       const int64_t vr = vec_row(g, w.bh, w.i, w.r0 / BT) + row;
       const float lse2_r = p.lse2[vr];     // +inf past the block end: P = 0
       const float dvec_r = p.dvec[vr];
@@ -560,32 +656,38 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         if (!block_visited(g, w.i, j)) continue;
         const int last = kt_last(g, w.i, j, w.r0);
         const int lim = key_limit(g, w.i, j, rq);
-        for (int kt = 0; kt <= last; ++kt) {
+        for (int kt = 0; kt <= last && ok; ++kt) {
           if (!(ok = mbar_wait(&bars->s_full, s_ph, wc, ST_BWD_WAIT | 0x18))) break;
           s_ph ^= 1;
           tc_fence_after();
+          const uint32_t tS = T_S + lane_off + 64 * grp;
+          const uint32_t tDP = T_DP + lane_off + 64 * grp;
+          uint32_t sv[64], dpv[64];
+          tmem_ld32(tS, sv);
+          tmem_ld32(tS + 32, sv + 32);
+          tmem_ld32(tDP, dpv);
+          tmem_ld32(tDP + 32, dpv + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->s_free);
           const bool masked = tile_masked(g, w.i, j, kt, w.r0);
+          const int rk0 = kt * BT + 64 * grp;               // first key row handled here
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            const int c0 = half * 64 + ch * 32;
-            uint32_t sv[32], dpv[32];
-            tmem_ld32(T_S + lane_off + c0, sv);
-            tmem_ld32(T_DP + lane_off + c0, dpv);
-            tmem_ld_wait();
+          for (int hh = 0; hh < 2; ++hh) {
             uint32_t dk[16];
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
-              float p0 = hw_exp2(fmaf(__uint_as_float(sv[k]), sl2, -lse2_r));
-              float p1 = hw_exp2(fmaf(__uint_as_float(sv[k + 1]), sl2, -lse2_r));
+              const int c = hh * 32 + k;
+              float p0 = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2_r));
+              float p1 = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2_r));
               if (masked) {
-                const int rk = kt * BT + c0 + k;
-                if (rk >= lim) p0 = 0.f;
-                if (rk + 1 >= lim) p1 = 0.f;
+                if (rk0 + c >= lim) p0 = 0.f;
+                if (rk0 + c + 1 >= lim) p1 = 0.f;
               }
-              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[k]) - dvec_r),
-                                       p1 * (__uint_as_float(dpv[k + 1]) - dvec_r));
+              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[c]) - dvec_r),
+                                       p1 * (__uint_as_float(dpv[c + 1]) - dvec_r));
             }
-            tmem_st16(T_S + lane_off + half * 64 + ch * 16, dk);
+            tmem_st16(tDP + hh * 16, dk);   // dS over this group's own dP columns
           }
           tmem_st_wait();
           tc_fence_before();
@@ -593,12 +695,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
       }
       if (!ok) break;
-      // ---- epilogue: this half's 64 columns of the dQ row, / sqrt(d)
+      // ---- epilogue: this group's 64 columns of the dQ row, / sqrt(d)
       if (!(ok = mbar_wait(&bars->dq_full, dq_ph, wc, ST_BWD_WAIT | 0x19))) break;
       dq_ph ^= 1;
       tc_fence_after();
-      const int64_t grow = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
-      store_row_bf16(T_DQ + lane_off + half * 64, p.dQ + grow * HD + half * 64, p.inv_sqrt_d, rq < g.c, 64);
+      store_row_bf16(T_DQ + lane_off + grp * 64, p.dQ + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
     }
@@ -703,7 +804,8 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
   kv::dkv_kernel<<<grid, THREADS, kv::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, p);
+  q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.Q),
+                                                           static_cast<const __nv_bfloat16*>(a.dO), p);
   return cudaGetLastError();
 }
 

@@ -184,19 +184,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, 0, 1);
       uint32_t kv_it = 0, q_ph = 0, pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
       bool ok = true, first = true;
-      auto issue_s = [&](int q, int st) {
-        const uint32_t qa = sbase + OFF_Q + q * TILE_BYTES;
-        const uint32_t ka = sbase + OFF_K + st * TILE_BYTES;
+      uint64_t* s_full = bars->s_full;
+      auto issue_s = [=](int q, int st) {
+        const uint64_t dq0 = kmajor_desc(sbase + OFF_Q + q * TILE_BYTES, 0);
+        const uint64_t dk0 = kmajor_desc(sbase + OFF_K + st * TILE_BYTES, 0);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss(tmem + q * 128, kmajor_desc(qa, kk), kmajor_desc(ka, kk), IDESC_QK, kk > 0);
-        mma_commit(&bars->s_full[q]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + q * 128, sdesc_add(dq0, off), sdesc_add(dk0, off), IDESC_QK, kk > 0);
+        }
+        mma_commit(&s_full[q]);
       };
-      auto issue_pv = [&](int q, int st, uint32_t acc) {
-        const uint32_t va = sbase + OFF_V + st * TILE_BYTES;
+      auto issue_pv = [=](int q, int st, uint32_t acc) {
+        const uint64_t dv0 = vmn_desc(sbase + OFF_V + st * TILE_BYTES, 0);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, vmn_desc(va, kk), IDESC_PV, (kk > 0) | acc);
+          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, sdesc_add(dv0, kk * 16 * 128), IDESC_PV,
+                 (kk > 0) | acc);
       };
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
