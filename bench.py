@@ -34,11 +34,13 @@ sys.path.insert(0, ROOT)
 METRIC = "ring-order blockwise attn fwd+bwd TFLOP/s, % GB300 BF16 peak (S=128K)"
 UNIT = "TFLOP/s"
 
-# DRAM traffic per launch of the dominant kernel, from one ncu capture
+# DRAM traffic per launch of a kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was taken on: the hash of csrc/<file> at capture time.
 NCU_TRAFFIC = {
-    # "fwd_bf16.cu": {"sha256": "...", "workload": "long_128k", "bytes_per_launch": ...},
+    "fwd": {"sha256": "f513cc2d013e5a8c62b77b64de25270989a436b4687ea2eed353cf79ea53971c", "workload": "long_128k", "bytes_per_launch": (10.86 + 1.13) * 1e9},
+    "bwd_dkv": {"sha256": "580f1578054763139a07adcf7d41d139b35b5e20e6c8363b06ab83262fe896dc", "workload": "long_128k", "bytes_per_launch": (8.16 + 2.20) * 1e9},
+    "bwd_dq": {"sha256": "580f1578054763139a07adcf7d41d139b35b5e20e6c8363b06ab83262fe896dc", "workload": "long_128k", "bytes_per_launch": (34.87 + 1.08) * 1e9},
 }
 
 
@@ -232,6 +234,7 @@ def run_ours(args, w):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    ra.set_kernel_timing(True)   # the library records CUDA events around each of its kernels
     with ClockSampler(local) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -240,7 +243,12 @@ def run_ours(args, w):
             step(True)
         t1.record(stream)
         torch.cuda.synchronize()
+    ktimes = ra.kernel_times()
+    ra.set_kernel_timing(False)
     ra.check_device_status()
+    per_kernel = {}
+    for name, ms in ktimes:
+        per_kernel.setdefault(name, []).append(ms)
     total_ms = t0.elapsed_time(t1)
     if ws > 1:
         tt = torch.tensor([total_ms], device="cuda")
@@ -294,16 +302,29 @@ def run_ours(args, w):
         e2e_ms = float(tt.item())
 
     burst, sustained, src = _peaks()
-    dom_is_bwd = with_bwd and bwd_ms is not None and bwd_ms > fwd_ms
-    dom_ms = bwd_ms if dom_is_bwd else fwd_ms
-    dom_flops = f_bwd if dom_is_bwd else f_fwd
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    src_file = "bwd_bf16.cu" if dom_is_bwd else "fwd_bf16.cu"
-    tr = NCU_TRAFFIC.get(src_file)
+    # Algorithmic FLOPs per launch of each tensor-core kernel.  The backward's
+    # five GEMMs (S, dP, dV, dK, dQ; 2.5x the forward's two) split as four in
+    # the dK/dV kernel and one (dQ) in the dQ kernel, which also recomputes S
+    # and dP (executed: three GEMMs).
+    gemm = f_fwd / 2
+    algo = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 1 * gemm}
+    executed = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 3 * gemm}
+    kernels = {}
+    for name, lst in per_kernel.items():
+        mean_ms = statistics.mean(lst)
+        kernels[name] = {"launches": len(lst), "ms": mean_ms}
+        if name in algo:
+            kernels[name]["tflops_algorithmic"] = algo[name] / (mean_ms * 1e-3) / 1e12
+            kernels[name]["tflops_executed"] = executed[name] / (mean_ms * 1e-3) / 1e12
+    dom = max((n for n in kernels if n in algo), key=lambda n: kernels[n]["ms"])
+    achieved = kernels[dom]["tflops_algorithmic"]
+    src_file = {"fwd": "fwd_bf16.cu", "bwd_dkv": "bwd_bf16.cu", "bwd_dq": "bwd_bf16.cu"}[dom]
+    tr = NCU_TRAFFIC.get(dom)
     traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash(src_file) and \
         tr["workload"] == args.workload else None
-    roofline = {"bound": "tensor", "kernel": "bwd" if dom_is_bwd else "fwd", "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved,
                 "peak": sustained, "unit": UNIT, "frac": achieved / sustained, "traffic": traffic,
+                "algorithmic_flops_per_launch": algo[dom], "avg_launch_ms": kernels[dom]["ms"],
                 "peak_kind": f"{src} sustained bf16 (burst {burst})", "frac_of_burst": achieved / burst}
 
     line = {
@@ -322,7 +343,8 @@ def run_ours(args, w):
         "roofline": roofline,
         "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (1 + (3 if with_bwd else 0)),
+        "kernels": kernels,
+        "gpu_launches": len(ktimes),
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -187,6 +187,29 @@ RA_API int ra_bwd_noalloc(const void* Q, const void* K, const void* V, const voi
 RA_API int ra_set_timing_buffer(uint64_t* dev_buf, size_t n);
 
 /*
+ * Kernel timing (opt-in measurement aid).  ra_set_kernel_timing(1) makes every
+ * later ra_fwd / ra_bwd call, from any thread, record CUDA events on its own
+ * stream immediately before and after each kernel it launches; 0 turns it off
+ * and drops unread records.  ra_kernel_times() waits for the recorded events,
+ * writes one record per timed kernel (oldest call first) and releases them:
+ *   call RA_CALL_FWD: kernel 0 = the forward kernel;
+ *   call RA_CALL_BWD: kernel 0 = preprocess (D_vec, LSE*log2e),
+ *                     kernel 1 = dK/dV kernel, kernel 2 = dQ kernel.
+ * `ms` is the event-to-event time in milliseconds.  *count receives the number
+ * of records; if it exceeds `capacity`, the first `capacity` are written, the
+ * rest are dropped and RA_ERR_ARG is returned.  The library creates (and keeps
+ * for reuse) the events; no device memory is allocated.
+ */
+typedef enum { RA_CALL_FWD = 0, RA_CALL_BWD = 1 } ra_call_kind;
+typedef struct {
+  int call;     /* ra_call_kind */
+  int kernel;   /* index inside the call, see above */
+  float ms;     /* duration, or -1 if it could not be measured */
+} ra_kernel_time;
+RA_API int ra_set_kernel_timing(int enable);
+RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
+
+/*
  * ra_check_device_status -- synchronise `stream`, then read and clear the
  * library's device-side status word.  Returns RA_ERR_TIMEOUT if any kernel
  * launched since the previous check gave up a bounded wait (the kernel then

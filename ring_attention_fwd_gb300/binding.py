@@ -35,6 +35,8 @@ SIGNATURES = {
                               _int, _int, _int, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
+    "ra_set_kernel_timing": (_int, [_int]),
+    "ra_kernel_times": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_int)]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),
 }
@@ -174,6 +176,29 @@ def set_timing_buffer(buf):
     else:
         _need(buf, "timing buffer")
         _check(lib().ra_set_timing_buffer(buf.data_ptr(), buf.numel()))
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("call", ctypes.c_int), ("kernel", ctypes.c_int), ("ms", ctypes.c_float)]
+
+
+KERNEL_NAMES = {(0, 0): "fwd", (1, 0): "bwd_prep", (1, 1): "bwd_dkv", (1, 2): "bwd_dq"}
+
+
+def set_kernel_timing(enable: bool):
+    """Record CUDA events around every later kernel of fwd/bwd calls (see
+    kernel_times)."""
+    _check(lib().ra_set_kernel_timing(int(bool(enable))))
+
+
+def kernel_times(capacity: int = 4096):
+    """Per-kernel durations of the calls timed since the last read: a list of
+    (name, ms), oldest first.  Waits for the recorded events."""
+    buf = (KernelTime * capacity)()
+    n = ctypes.c_int(0)
+    _check(lib().ra_kernel_times(ctypes.addressof(buf), capacity, ctypes.byref(n)))
+    return [(KERNEL_NAMES.get((buf[k].call, buf[k].kernel), f"{buf[k].call}.{buf[k].kernel}"), buf[k].ms)
+            for k in range(n.value)]
 
 
 def check_device_status(stream=None):

@@ -785,6 +785,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   const CUtensorMap& mdo = *static_cast<const CUtensorMap*>(tmap_do);
 
   const int64_t prow = a.B * a.H * a.N * p.g.n_mb * BT;   // padded query rows
+  if (a.ev) cudaEventRecord(a.ev[0], a.stream);
   prep_kernel<<<static_cast<unsigned>((prow * 32 + 255) / 256), 256, 0, a.stream>>>(
       static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.LSE, a.lse2, a.dvec, p.g,
       p.S, prow);
@@ -802,11 +803,15 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   const int64_t units = a.B * a.H * a.N * p.g.n_kt;   // KV tiles = query tiles
   p.num_units = units;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
+  if (a.ev) cudaEventRecord(a.ev[1], a.stream);
   kv::dkv_kernel<<<grid, THREADS, kv::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ev) cudaEventRecord(a.ev[2], a.stream);
   q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.Q),
                                                            static_cast<const __nv_bfloat16*>(a.dO), p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (a.ev) cudaEventRecord(a.ev[3], a.stream);
+  return e;
 }
 
 }  // namespace ra

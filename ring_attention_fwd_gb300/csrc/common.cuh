@@ -141,6 +141,7 @@ struct FwdArgs {
   unsigned long long* timing;  // [N*N] or null
   cudaStream_t stream;
   int num_sms;
+  cudaEvent_t* ev;             // null, or 2 events recorded before/after the kernel
 };
 cudaError_t launch_fwd_f32(const FwdArgs& a);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tmap_k,
@@ -165,6 +166,7 @@ struct BwdArgs {
   unsigned int* status;
   cudaStream_t stream;
   int num_sms;
+  cudaEvent_t* ev;   // null, or 4 events: before prep, dK/dV and dQ kernels, and after
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v, const void* tmap_do);

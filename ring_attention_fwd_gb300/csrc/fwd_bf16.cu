@@ -411,10 +411,13 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   }
   const int64_t grid64 = p.num_units < a.num_sms ? p.num_units : a.num_sms;
   const int grid = static_cast<int>(grid64 > 0 ? grid64 : 1);
+  if (a.ev) cudaEventRecord(a.ev[0], a.stream);
   fwd_kernel<<<grid, THREADS, SMEM_BYTES, a.stream>>>(*static_cast<const CUtensorMap*>(tmap_q),
                                                        *static_cast<const CUtensorMap*>(tmap_k),
                                                        *static_cast<const CUtensorMap*>(tmap_v), p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (a.ev) cudaEventRecord(a.ev[1], a.stream);
+  return e;
 }
 
 }  // namespace ra

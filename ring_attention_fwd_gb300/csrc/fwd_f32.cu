@@ -167,8 +167,11 @@ cudaError_t launch_fwd_f32(const FwdArgs& a) {
   }
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
   const int grid = static_cast<int>(p.num_units < cap ? p.num_units : cap);
+  if (a.ev) cudaEventRecord(a.ev[0], a.stream);
   fwd_f32_kernel<<<grid > 0 ? grid : 1, THREADS, smem, a.stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (a.ev) cudaEventRecord(a.ev[1], a.stream);
+  return e;
 }
 
 }  // namespace ra

@@ -9,8 +9,11 @@
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
+#include <deque>
+#include <map>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/ringattn.h"
 #include "common.cuh"
@@ -71,6 +74,45 @@ int device_state(DevState** out) {
 
 std::atomic<uint64_t*> g_timing_buf{nullptr};
 std::atomic<size_t> g_timing_n{0};
+
+// ------------------------------------------------------- kernel timing (opt-in)
+// While enabled, each ra_fwd / ra_bwd call records CUDA events on its stream
+// around its kernels; ra_kernel_times() reads and releases them.
+struct TimedCall {
+  int call;           // ra_call_kind
+  int nk;             // kernels timed (events = nk + 1)
+  int dev;
+  cudaEvent_t ev[4];
+};
+std::atomic<bool> g_kt_on{false};
+std::mutex g_kt_mu;
+std::deque<TimedCall> g_kt_calls;
+std::map<int, std::vector<cudaEvent_t>> g_kt_pool;   // idle events per device
+
+// Events for one call of `nk` kernels on the current device, or null when
+// timing is off (or an event cannot be created: the call then runs untimed).
+cudaEvent_t* kt_begin(int call, int nk) {
+  if (!g_kt_on.load()) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(g_kt_mu);
+  TimedCall tc{call, nk, dev, {}};
+  auto& pool = g_kt_pool[dev];
+  for (int k = 0; k <= nk; ++k) {
+    if (pool.empty()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) {
+        for (int m = 0; m < k; ++m) pool.push_back(tc.ev[m]);
+        return nullptr;
+      }
+      pool.push_back(e);
+    }
+    tc.ev[k] = pool.back();
+    pool.pop_back();
+  }
+  g_kt_calls.push_back(tc);
+  return g_kt_calls.back().ev;
+}
 
 // ---------------------------------------------------------------- TMA maps
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -143,6 +185,44 @@ int ra_set_timing_buffer(uint64_t* dev_buf, size_t n) {
   return RA_OK;
 }
 
+int ra_set_kernel_timing(int enable) {
+  if (enable != 0 && enable != 1) return fail(RA_ERR_ARG, "ra_set_kernel_timing: enable must be 0 or 1");
+  std::lock_guard<std::mutex> lk(g_kt_mu);
+  g_kt_on.store(enable == 1);
+  if (!enable) {   // pending records are dropped; their events go back to the pool
+    for (auto& c : g_kt_calls)
+      for (int k = 0; k <= c.nk; ++k) g_kt_pool[c.dev].push_back(c.ev[k]);
+    g_kt_calls.clear();
+  }
+  return RA_OK;
+}
+
+int ra_kernel_times(ra_kernel_time* out, int capacity, int* count) {
+  if (!count || (capacity > 0 && !out) || capacity < 0) return fail(RA_ERR_ARG, "ra_kernel_times: bad arguments");
+  std::lock_guard<std::mutex> lk(g_kt_mu);
+  int n = 0, rc = RA_OK;
+  for (auto& c : g_kt_calls) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != c.dev) cudaSetDevice(c.dev);
+    cudaError_t e = cudaEventSynchronize(c.ev[c.nk]);
+    for (int k = 0; k < c.nk; ++k) {
+      float ms = -1.f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, c.ev[k], c.ev[k + 1]);
+      if (n < capacity) out[n] = ra_kernel_time{c.call, k, ms};
+      ++n;
+    }
+    if (prev != c.dev) cudaSetDevice(prev);
+    if (e != cudaSuccess && rc == RA_OK) rc = cuda_fail(e, "ra_kernel_times");
+    for (int k = 0; k <= c.nk; ++k) g_kt_pool[c.dev].push_back(c.ev[k]);
+  }
+  g_kt_calls.clear();
+  *count = n;
+  if (rc == RA_OK && n > capacity)
+    rc = fail(RA_ERR_ARG, "ra_kernel_times: %d records, room for %d (the rest were dropped)", n, capacity);
+  return rc;
+}
+
 int ra_check_device_status(void* stream) {
   DevState* d = nullptr;
   int rc = device_state(&d);
@@ -194,6 +274,7 @@ int ra_fwd(const void* Q, const void* K, const void* V, int64_t B, int64_t H, in
   a.timing = reinterpret_cast<unsigned long long*>(timing);
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
+  a.ev = kt_begin(RA_CALL_FWD, 1);
   cudaError_t e;
   if (dtype == RA_BF16) {
     CUtensorMap mq, mk, mv;
@@ -295,6 +376,7 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
   if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mdo, dO, B * H, S, D, 128)) != RA_OK) return rc;
+  a.ev = kt_begin(RA_CALL_BWD, 3);
   cudaError_t e = ra::launch_bwd_bf16(a, &mq, &mk, &mv, &mdo);
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: kernel not built");
   if (e != cudaSuccess) return cuda_fail(e, "ra_bwd launch");

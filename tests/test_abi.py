@@ -27,7 +27,7 @@ def declared_symbols():
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
-        "ra_check_device_status", "ra_last_error", "ra_version"])
+        "ra_set_kernel_timing", "ra_kernel_times", "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -114,6 +114,14 @@ def test_bwd_noalloc_rejects_sizes_before_touching_a_gpu(L):
                                 None)
     assert call(1, 1, 100, 3) == 1 and "invalid sizes" in L.ra_last_error().decode()
     assert call(1, 64, 131072, 32) == 1 and "more than the fixed" in L.ra_last_error().decode()
+
+
+def test_kernel_timing_arguments(L):
+    n = ctypes.c_int(-1)
+    assert L.ra_set_kernel_timing(2) == 1
+    assert L.ra_kernel_times(None, -1, ctypes.byref(n)) == 1
+    assert L.ra_kernel_times(None, 0, ctypes.byref(n)) == 0 and n.value == 0   # nothing recorded
+    assert L.ra_set_kernel_timing(0) == 0
 
 
 def test_timing_buffer_arguments(L):

@@ -124,3 +124,20 @@ def test_per_device_timing_buffer(ra):
         for s in range(N):
             j = (i - s) % N
             assert (t[i, s] > 0) == (j <= i), (i, s, t)
+
+
+def test_kernel_timing_records(ra):
+    """Opt-in kernel timing: one record per kernel of every timed call, in
+    order, with positive durations; nothing is recorded once it is off."""
+    inp = {k: v.cuda() for k, v in make_inputs(1, 2, 1024, 128, seed=12, with_grad=True).items()}
+    ra.set_kernel_timing(True)
+    try:
+        o, lse = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
+        ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped")
+        t = ra.kernel_times()
+    finally:
+        ra.set_kernel_timing(False)
+    assert [n for n, _ in t] == ["fwd", "bwd_prep", "bwd_dkv", "bwd_dq"]
+    assert all(ms > 0 for _, ms in t)
+    ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
+    assert ra.kernel_times() == []
