@@ -359,6 +359,58 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
 
 
+def run_balance(args):
+    """Per-virtual-host work and time of the forward, striped vs contiguous
+    (the 32768-token, 16-block workload by default): analytic visible-pair
+    FLOPs per block, CTA-time per (block, ring step) from the kernel's
+    %globaltimer hooks, and the makespan of N hosts that each ran their block
+    alone on a GPU like this one (sum over ring steps of the slowest host;
+    no communication).  Prints one JSON line."""
+    import torch
+    import ring_attention_fwd_gb300 as ra
+    from ring_attention_fwd_gb300 import flops as fl
+    from ring_attention_fwd_gb300.inputs import WORKLOADS, make_inputs
+    w = dict(WORKLOADS[args.workload])
+    B, H, S, D, N = w["B"], w["H"], w["S"], w["D"], w["N"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    inp = {k: v.cuda() for k, v in make_inputs(B, H, S, D, w["seed"], scale=w["scale"]).items()}
+    out = {"workload": args.workload, "B": B, "H": H, "S": S, "D": D, "N": N, "causal": True, "layouts": {}}
+    buf = torch.zeros(N * N, dtype=torch.int64, device="cuda")
+    for layout in ("contiguous", "striped"):
+        for _ in range(args.warmup):
+            ra.fwd(inp["q"], inp["k"], inp["v"], N, True, layout)
+        times, kms = [], []
+        for _ in range(args.steps):
+            buf.zero_()
+            ra.set_timing_buffer(buf)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ra.fwd(inp["q"], inp["k"], inp["v"], N, True, layout)
+            e1.record()
+            torch.cuda.synchronize()
+            ra.set_timing_buffer(None)
+            times.append(buf.view(N, N).double().cpu())
+            kms.append(e0.elapsed_time(e1))
+        ra.check_device_status()
+        t = sum(times) / len(times) / 1e6                  # CTA-ms per (block, ring step)
+        pairs = fl.visible_pairs_per_block(S, N, layout, True)
+        per_dev_ms = (t.sum(dim=1) / sms).tolist()         # block i alone on all SMs
+        makespan = float((t.max(dim=0).values / sms).sum())
+        out["layouts"][layout] = {
+            "flops_per_block": [4 * D * H * B * p for p in pairs],
+            "flops_max_over_min": max(pairs) / min(pairs),
+            "time_ms_per_block": per_dev_ms,
+            "time_max_over_min": max(per_dev_ms) / min(per_dev_ms),
+            "simulated_makespan_ms": makespan,
+            "kernel_ms": statistics.mean(kms),
+        }
+    L = out["layouts"]
+    out["striped_speedup_of_simulated_makespan"] = (L["contiguous"]["simulated_makespan_ms"] /
+                                                    L["striped"]["simulated_makespan_ms"])
+    out["pages_context"] = "striped 1.45x at 256K, 1.65x at 786K tokens, multi-device, hardware not stated"
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,10 +420,17 @@ def main():
     ap.add_argument("--workload", default="long_128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--balance", action="store_true",
+                    help="report per-virtual-host work and time, striped vs contiguous (default workload balance_32k)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from ring_attention_fwd_gb300.inputs import WORKLOADS
+    if args.balance:
+        if args.workload == "long_128k" and "--workload" not in sys.argv:
+            args.workload = "balance_32k"
+        run_balance(args)
+        return
     w = dict(WORKLOADS[args.workload])
     if args.impl == "reference":
         run_reference(args, w)

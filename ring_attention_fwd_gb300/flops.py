@@ -25,6 +25,21 @@ def bwd_flops(B: int, H: int, S: int, D: int, causal: bool) -> int:
     return fwd_flops(B, H, S, D, causal) * 5 // 2
 
 
+def visible_pairs_per_block(S: int, N: int, layout: str, causal: bool) -> list:
+    """Visible (query, key) pairs whose query lies in block i (virtual host i).
+
+    Causal, contiguous: block i holds tokens i*c .. i*c+c-1, token t sees t+1
+    keys, so i*c^2 + c(c+1)/2.  Causal, striped: block i holds tokens r*N + i,
+    so N*c(c-1)/2 + c(i+1).  Non-causal: c*S for every block.
+    """
+    c = S // N
+    if not causal:
+        return [c * S] * N
+    if layout == "contiguous":
+        return [i * c * c + c * (c + 1) // 2 for i in range(N)]
+    return [N * c * (c - 1) // 2 + c * (i + 1) for i in range(N)]
+
+
 def kv_block_bytes(c: int, d: int, elem_bytes: int = 2) -> int:
     """Bytes of one K block plus one V block of c rows: 2*c*d*elem (4cd in bf16)."""
     return 2 * c * d * elem_bytes

@@ -341,6 +341,15 @@ def test_kv_rows_match_full_backward():
 
 
 # ------------------------------------------------------------- work per device
+def test_product_pair_counter_matches_oracle():
+    from ring_attention_fwd_gb300 import flops
+    for S, N in ((16, 4), (96, 3), (2048, 16)):
+        for layout in LAYOUTS:
+            for causal in (True, False):
+                assert flops.visible_pairs_per_block(S, N, layout, causal) == \
+                    orc.visible_pairs_per_device(S, N, layout, causal).tolist()
+
+
 def test_visible_pairs_brute_force_and_balance():
     for S, N in ((16, 4), (64, 8), (96, 3)):
         for layout in LAYOUTS:
