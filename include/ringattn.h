@@ -88,6 +88,29 @@ RA_API int ra_fwd(const void* Q, const void* K, const void* V,
            void* O, float* LSE, void* stream);
 
 /*
+ * ra_fwd_step -- one step of one ring host: query block i against KV block j.
+ *
+ * The per-host operation of a multi-device ring ([CH] §5.2: each host keeps
+ * Q_i and, every round, attends it to the K_j, V_j it currently holds while
+ * forwarding them; [FT] "Ring Attention的核心洞察" steps 3-4).  Returns the
+ * partial state over block j's keys only: O normalised over those keys and
+ * LSE = ln sum over them; rows that see none of them get O = 0, LSE = -inf.
+ * Chaining the N steps of a host with ra_merge gives that host's rows of
+ * ra_fwd.  The mask uses the true token positions of blocks i and j under
+ * `layout` (contiguous causal j > i: all masked, no kernel runs).
+ *
+ *   Q_i, K_j, V_j : [B,H,c,D] of `dtype` (the blocks, not the whole sequence).
+ *   O : [B,H,c,D] of `dtype` (output);  LSE : [B,H,c] float32 (output).
+ *   N : ring size; i, j : block indices in [0, N).  Other arguments and errors
+ *   as for ra_fwd (with S = c and one block).
+ */
+RA_API int ra_fwd_step(const void* Q_i, const void* K_j, const void* V_j,
+           int64_t B, int64_t H, int64_t c, int64_t D,
+           int64_t N, int64_t i, int64_t j,
+           int causal, int layout, int dtype,
+           void* O, float* LSE, void* stream);
+
+/*
  * ra_merge -- LogSumExp merge of two partial states over disjoint key sets,
  * in place into (O_a, lse_a)  ([FT] "Online Softmax": l = l1 e^{m1-m} +
  * l2 e^{m2-m} and its log-space form).  Per row:

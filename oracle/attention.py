@@ -204,6 +204,33 @@ def ring_attention(q, k, v, n_blocks: int, causal: bool, layout: str, order_fn=N
     return o, lse
 
 
+def block_pair_attention(q, k, v, i: int, j: int, n_blocks: int, causal: bool, layout: str):
+    """Partial state of query block i over the keys of block j only, ONE head.
+
+    What host i holds after attending its queries to the one KV block j it
+    has in a ring round ([CH] §5.2): softmax over block j's visible keys.
+    q, k, v: float64 [S, D] of the whole sequence (storage order), so that the
+    token positions of both blocks are those of `layout`.  Rows that see none
+    of block j's keys get O = 0, LSE = -inf.  Returns (o [c, D], lse [c]).
+    """
+    S, D = k.shape
+    c = S // n_blocks
+    pos = token_positions(S, n_blocks, layout)
+    qi = q[i * c:(i + 1) * c]
+    kj, vj = k[j * c:(j + 1) * c], v[j * c:(j + 1) * c]
+    s = (qi @ kj.T) / np.sqrt(D)
+    s = np.where(visible(pos[i * c:(i + 1) * c], pos[j * c:(j + 1) * c], causal), s, -np.inf)
+    m = s.max(axis=1)
+    seen = np.isfinite(m)
+    e = np.exp(s - np.where(seen, m, 0.0)[:, None])
+    l = e.sum(axis=1)
+    o = np.zeros((c, D))
+    o[seen] = (e[seen] @ vj) / l[seen, None]
+    lse = np.full(c, -np.inf)
+    lse[seen] = m[seen] + np.log(l[seen])
+    return o, lse
+
+
 # ----------------------------------------------------------------------------
 # LogSumExp merge of two partial states
 # ----------------------------------------------------------------------------

@@ -27,6 +27,8 @@ _DTYPE = {torch.float32: RA_F32, torch.bfloat16: RA_BF16}
 _i64, _vp, _fp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "ra_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp, _vp]),
+    "ra_fwd_step": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp,
+                           _vp]),
     "ra_merge": (_int, [_vp, _fp, _vp, _fp, _i64, _i64, _int, _vp]),
     "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -105,6 +107,24 @@ def fwd(q, k, v, n_blocks: int, causal: bool = True, layout: str = "contiguous",
     _check(lib().ra_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, S, D, int(n_blocks),
                         int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], o.data_ptr(), lse.data_ptr(),
                         _stream_ptr(stream)))
+    return o, lse
+
+
+def fwd_step(q_i, k_j, v_j, n_blocks: int, i: int, j: int, causal: bool = True, layout: str = "contiguous", *,
+             o=None, lse=None, stream=None):
+    """One ring step of host i: its query block q_i [B, H, c, D] against KV
+    block j (k_j, v_j of the same shape).  Returns the partial (o, lse) over
+    block j's keys; chain the steps with merge()."""
+    for name, t in (("q_i", q_i), ("k_j", k_j), ("v_j", v_j)):
+        _need(t, name, q_i.dtype)
+    B, H, c, D = q_i.shape
+    if o is None:
+        o = torch.empty_like(q_i)
+    if lse is None:
+        lse = torch.empty((B, H, c), dtype=torch.float32, device=q_i.device)
+    _check(lib().ra_fwd_step(q_i.data_ptr(), k_j.data_ptr(), v_j.data_ptr(), B, H, c, D, int(n_blocks), int(i),
+                             int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype], o.data_ptr(),
+                             lse.data_ptr(), _stream_ptr(stream)))
     return o, lse
 
 

@@ -766,6 +766,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.g.c = static_cast<int>(a.S / a.N);
   p.g.causal = a.causal;
   p.g.striped = a.striped;
+  p.g.strict = 0;
   p.g.kt_w = BT;
   p.g.n_kt = (p.g.c + BT - 1) / BT;
   p.g.mb_h = BT;

@@ -19,6 +19,8 @@ struct RingGeom {
   int n_kt;     // KV tiles per block = ceil(c / kt_w)
   int mb_h;     // query rows per work unit
   int n_mb;     // work units per query block = ceil(c / mb_h)
+  int strict;   // 1: diag-type pairs never see the key at the query's own row
+                //    (one striped pair j > i evaluated as a 1-block problem)
 };
 
 // Ring order: at step s, query block i meets KV block (i - s) mod N (host i
@@ -45,7 +47,7 @@ __host__ __device__ __forceinline__ bool diag_type(const RingGeom& g, int i, int
 // contiguous j == i (same token), striped j <= i (token rk*N+j <= rq*N+i).
 // So rk is visible iff rk < rq + incl, with incl = 1 if (contiguous or j <= i).
 __host__ __device__ __forceinline__ int diag_incl(const RingGeom& g, int i, int j) {
-  return (!g.striped || j <= i) ? 1 : 0;
+  return (!g.strict && (!g.striped || j <= i)) ? 1 : 0;
 }
 
 // Last KV tile of block j that a unit of query rows [r0, r0 + mb_h) needs.
@@ -137,6 +139,7 @@ struct FwdArgs {
   float* LSE;
   int64_t B, H, S, D, N;
   int causal, striped;
+  int strict;                  // see RingGeom::strict (0 for whole-sequence calls)
   unsigned int* status;
   unsigned long long* timing;  // [N*N] or null
   cudaStream_t stream;
@@ -148,6 +151,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
                             const void* tmap_v);
 cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
                          int64_t D, int bf16, cudaStream_t stream, int num_sms);
+cudaError_t launch_fill(float* x, int64_t n, float value, cudaStream_t stream, int num_sms);
 
 struct BwdArgs {
   const void* Q;

@@ -392,6 +392,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   p.g.c = static_cast<int>(a.S / a.N);
   p.g.causal = a.causal;
   p.g.striped = a.striped;
+  p.g.strict = a.strict;
   p.g.kt_w = BN;
   p.g.n_kt = (p.g.c + BN - 1) / BN;
   p.g.mb_h = 2 * BM;

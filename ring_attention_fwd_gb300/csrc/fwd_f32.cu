@@ -143,6 +143,7 @@ cudaError_t launch_fwd_f32(const FwdArgs& a) {
   p.g.c = static_cast<int>(a.S / a.N);
   p.g.causal = a.causal;
   p.g.striped = a.striped;
+  p.g.strict = a.strict;
   p.g.kt_w = BN;
   p.g.n_kt = (p.g.c + BN - 1) / BN;
   p.g.mb_h = BM;

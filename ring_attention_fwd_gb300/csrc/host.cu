@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <deque>
@@ -166,6 +167,57 @@ int check_enums(int causal, int layout, int dtype) {
   return RA_OK;
 }
 
+// Validates and launches one forward over tensors of S rows cut into N blocks.
+// `strict` and `use_timing` serve ra_fwd_step (one block pair as a 1-block call).
+int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+             int causal, int layout, int dtype, void* O, float* LSE, void* stream, int strict, bool use_timing) {
+  if (!Q || !K || !V || !O || !LSE) return fail(RA_ERR_ARG, "ra_fwd: null pointer");
+  int rc = check_sizes(B, H, S, D, N);
+  if (rc != RA_OK) return rc;
+  if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
+  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd: LSE must be 4-byte aligned");
+  if (dtype == RA_BF16) {
+    if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_fwd: bf16 path needs D == 128 (got %lld)", (long long)D);
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+      return fail(RA_ERR_ARG, "ra_fwd: bf16 tensors must be 16-byte aligned");
+  } else {
+    if (D % 4 != 0 || D > 128)
+      return fail(RA_ERR_UNSUPPORTED, "ra_fwd: f32 path needs D %% 4 == 0 and D <= 128 (got %lld)", (long long)D);
+    if (!aligned(Q, 4) || !aligned(K, 4) || !aligned(V, 4) || !aligned(O, 4))
+      return fail(RA_ERR_ARG, "ra_fwd: f32 tensors must be 4-byte aligned");
+  }
+  uint64_t* timing = use_timing ? g_timing_buf.load() : nullptr;
+  if (timing && g_timing_n.load() < static_cast<size_t>(N * N))
+    return fail(RA_ERR_ARG, "timing buffer holds %zu entries, N*N = %lld needed", g_timing_n.load(),
+                (long long)(N * N));
+  DevState* d = nullptr;
+  if ((rc = device_state(&d)) != RA_OK) return rc;
+
+  ra::FwdArgs a;
+  a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE;
+  a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
+  a.causal = causal;
+  a.striped = layout == RA_STRIPED;
+  a.strict = strict;
+  a.status = d->status;
+  a.timing = reinterpret_cast<unsigned long long*>(timing);
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.num_sms = d->num_sms;
+  a.ev = kt_begin(RA_CALL_FWD, 1);
+  cudaError_t e;
+  if (dtype == RA_BF16) {
+    CUtensorMap mq, mk, mv;
+    if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
+    e = ra::launch_fwd_bf16(a, &mq, &mk, &mv);
+  } else {
+    e = ra::launch_fwd_f32(a);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "ra_fwd launch");
+  return RA_OK;
+}
+
 }  // namespace
 
 namespace ra {
@@ -241,52 +293,42 @@ int ra_check_device_status(void* stream) {
   return RA_OK;
 }
 
+
 int ra_fwd(const void* Q, const void* K, const void* V, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
            int causal, int layout, int dtype, void* O, float* LSE, void* stream) {
-  if (!Q || !K || !V || !O || !LSE) return fail(RA_ERR_ARG, "ra_fwd: null pointer");
-  int rc = check_sizes(B, H, S, D, N);
-  if (rc != RA_OK) return rc;
-  if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
-  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd: LSE must be 4-byte aligned");
-  if (dtype == RA_BF16) {
-    if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_fwd: bf16 path needs D == 128 (got %lld)", (long long)D);
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
-      return fail(RA_ERR_ARG, "ra_fwd: bf16 tensors must be 16-byte aligned");
-  } else {
-    if (D % 4 != 0 || D > 128)
-      return fail(RA_ERR_UNSUPPORTED, "ra_fwd: f32 path needs D %% 4 == 0 and D <= 128 (got %lld)", (long long)D);
-    if (!aligned(Q, 4) || !aligned(K, 4) || !aligned(V, 4) || !aligned(O, 4))
-      return fail(RA_ERR_ARG, "ra_fwd: f32 tensors must be 4-byte aligned");
-  }
-  uint64_t* timing = g_timing_buf.load();
-  if (timing && g_timing_n.load() < static_cast<size_t>(N * N))
-    return fail(RA_ERR_ARG, "timing buffer holds %zu entries, N*N = %lld needed", g_timing_n.load(),
-                (long long)(N * N));
-  DevState* d = nullptr;
-  if ((rc = device_state(&d)) != RA_OK) return rc;
+  return fwd_impl(Q, K, V, B, H, S, D, N, causal, layout, dtype, O, LSE, stream, 0, true);
+}
 
-  ra::FwdArgs a;
-  a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE;
-  a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
-  a.causal = causal;
-  a.striped = layout == RA_STRIPED;
-  a.status = d->status;
-  a.timing = reinterpret_cast<unsigned long long*>(timing);
-  a.stream = static_cast<cudaStream_t>(stream);
-  a.num_sms = d->num_sms;
-  a.ev = kt_begin(RA_CALL_FWD, 1);
-  cudaError_t e;
-  if (dtype == RA_BF16) {
-    CUtensorMap mq, mk, mv;
-    if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
-    if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
-    if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
-    e = ra::launch_fwd_bf16(a, &mq, &mk, &mv);
-  } else {
-    e = ra::launch_fwd_f32(a);
+int ra_fwd_step(const void* Q_i, const void* K_j, const void* V_j, int64_t B, int64_t H, int64_t c, int64_t D,
+                int64_t N, int64_t i, int64_t j, int causal, int layout, int dtype, void* O, float* LSE,
+                void* stream) {
+  if (N < 1 || i < 0 || i >= N || j < 0 || j >= N)
+    return fail(RA_ERR_ARG, "ra_fwd_step: need 0 <= i, j < N (i=%lld j=%lld N=%lld)", (long long)i, (long long)j,
+                (long long)N);
+  int rc = check_enums(causal, layout, dtype);
+  if (rc != RA_OK) return rc;
+  const bool striped = layout == RA_STRIPED;
+  if (causal && !striped && j > i) {
+    // Every key of block j comes after every query of block i: the partial is
+    // empty (O = 0, LSE = -inf), which ra_merge treats as "no keys".
+    if (!Q_i || !K_j || !V_j || !O || !LSE) return fail(RA_ERR_ARG, "ra_fwd_step: null pointer");
+    if ((rc = check_sizes(B, H, c, D, 1)) != RA_OK) return rc;
+    if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd_step: LSE must be 4-byte aligned");
+    DevState* d = nullptr;
+    if ((rc = device_state(&d)) != RA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t esz = dtype == RA_BF16 ? 2 : 4;
+    cudaError_t e = cudaMemsetAsync(O, 0, static_cast<size_t>(B * H * c * D) * esz, st);
+    if (e == cudaSuccess) e = ra::launch_fill(LSE, B * H * c, -INFINITY, st, d->num_sms);
+    if (e != cudaSuccess) return cuda_fail(e, "ra_fwd_step fill");
+    return RA_OK;
   }
-  if (e != cudaSuccess) return cuda_fail(e, "ra_fwd launch");
-  return RA_OK;
+  // One block pair as a 1-block problem: a per-element mask only on
+  // diagonal-type pairs; a striped pair with j > i also hides the key at the
+  // query's own row (that key is a later token).
+  const int pair_causal = (causal && (striped || j == i)) ? 1 : 0;
+  const int strict = (causal && striped && j > i) ? 1 : 0;
+  return fwd_impl(Q_i, K_j, V_j, B, H, c, D, 1, pair_causal, layout, dtype, O, LSE, stream, strict, false);
 }
 
 int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows, int64_t D, int dtype,

@@ -90,7 +90,21 @@ cudaError_t run(void* O_a, float* lse_a, const void* O_b, const float* lse_b, in
   return cudaGetLastError();
 }
 
+__global__ void fill_kernel(float* x, int64_t n, float value) {
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    x[k] = value;
+}
+
 }  // namespace mrg
+
+cudaError_t launch_fill(float* x, int64_t n, float value, cudaStream_t stream, int num_sms) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+  mrg::fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, n, value);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
                          int64_t D, int bf16, cudaStream_t stream, int /*num_sms*/) {

@@ -1,0 +1,71 @@
+"""Ring forward across processes: one query block per rank, K/V blocks rotate.
+
+The multi-device form of the method ("Ring Attention with Blockwise
+Transformers for Near Infinite Context" notes, §5.2; "Ring Attention如何让大模型
+突破百万Token上下文…", "Ring Attention的核心洞察" steps 1-5): rank i of an N-rank
+group holds query block i and KV block i.  In round s it attends its queries
+to the KV block it holds -- block (i - s) mod N -- while sending that block to
+rank i+1 and receiving the next one from rank i-1, so the transfer overlaps
+the compute.  After N rounds every rank has seen every KV block; the partial
+states are folded with the LogSumExp merge.  Contiguous causal rounds whose
+block lies entirely in the future (j > i) are skipped (the block is still
+forwarded).
+
+The block compute and the merge default to the library's ``fwd_step`` and
+``merge`` (CUDA tensors, NCCL process group).  Both are parameters, so the
+exchange protocol can be exercised elsewhere with other implementations.
+"""
+from __future__ import annotations
+
+import datetime
+
+import torch
+import torch.distributed as dist
+
+
+def ring_order(i: int, n: int):
+    """KV block held by rank i in rounds 0..n-1: i, i-1, ... (mod n)."""
+    return [(i - s) % n for s in range(n)]
+
+
+def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", group=None, step=None,
+                 merge=None, timeout_s: float | None = None):
+    """Ring attention forward for this rank's block.
+
+    q, k, v: this rank's blocks [B, H, c, D] (block index = rank in `group`).
+    step(q, k_j, v_j, n, i, j) -> (o, lse): partial state of block i over
+    block j; merge(o, lse, o_j, lse_j) folds a partial into (o, lse) in place.
+    timeout_s: give up (RuntimeError) if a round's exchange has not completed
+    within this many seconds, instead of waiting for a peer that is gone.
+    Returns (o, lse) of this rank's query rows.
+    """
+    n = dist.get_world_size(group)
+    i = dist.get_rank(group)
+    if step is None or merge is None:
+        from . import binding
+        step = step or (lambda qq, kk, vv, nn, ii, jj: binding.fwd_step(qq, kk, vv, nn, ii, jj, causal, layout))
+        merge = merge or (lambda o, l, oj, lj: binding.merge(o, l, oj, lj))
+    send_to, recv_from = (i + 1) % n, (i - 1) % n
+    bufs = [(torch.empty_like(k), torch.empty_like(v)) for _ in range(2 if n > 1 else 0)]
+    cur_k, cur_v = k, v
+    o = lse = None
+    for s, j in enumerate(ring_order(i, n)):
+        reqs = []
+        if s < n - 1:   # forward the block we hold, receive the next one
+            nk, nv = bufs[s % 2]
+            ops = [dist.P2POp(dist.isend, cur_k, send_to, group), dist.P2POp(dist.irecv, nk, recv_from, group),
+                   dist.P2POp(dist.isend, cur_v, send_to, group), dist.P2POp(dist.irecv, nv, recv_from, group)]
+            reqs = dist.batch_isend_irecv(ops)
+        if not (causal and layout == "contiguous" and j > i):
+            oj, lj = step(q, cur_k, cur_v, n, i, j)
+            if o is None:
+                o, lse = oj, lj
+            else:
+                merge(o, lse, oj, lj)
+        for r in reqs:
+            ok = r.wait(datetime.timedelta(seconds=timeout_s)) if timeout_s is not None else r.wait()
+            if ok is False:
+                raise RuntimeError(f"ring round {s}: exchange with ranks {recv_from}/{send_to} timed out")
+        if s < n - 1:
+            cur_k, cur_v = bufs[s % 2]
+    return o, lse

@@ -26,7 +26,7 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
-        "ra_fwd", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
+        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
         "ra_set_kernel_timing", "ra_kernel_times", "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
@@ -114,6 +114,15 @@ def test_bwd_noalloc_rejects_sizes_before_touching_a_gpu(L):
                                 None)
     assert call(1, 1, 100, 3) == 1 and "invalid sizes" in L.ra_last_error().decode()
     assert call(1, 64, 131072, 32) == 1 and "more than the fixed" in L.ra_last_error().decode()
+
+
+def test_fwd_step_rejects_bad_block_indices(L):
+    def call(N, i, j):
+        return L.ra_fwd_step(FAKE, FAKE, FAKE, 1, 1, 64, 128, N, i, j, 1, 0, 1, FAKE, FAKE, None)
+    assert call(4, 4, 0) == 1 and "0 <= i, j < N" in L.ra_last_error().decode()
+    assert call(4, 0, -1) == 1
+    assert call(0, 0, 0) == 1
+    assert L.ra_fwd_step(None, FAKE, FAKE, 1, 1, 64, 128, 4, 1, 0, 1, 0, 1, FAKE, FAKE, None) == 1
 
 
 def test_kernel_timing_arguments(L):

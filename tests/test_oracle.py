@@ -215,6 +215,29 @@ def test_merge_of_key_halves_equals_whole():
     assert np.allclose(np.exp(lm), np.exp(la) + np.exp(lb), rtol=1e-13)
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_pair_partials_merge_to_the_whole(layout, causal):
+    """Host i's N partial states (one per KV block it meets on the ring),
+    folded with the merge, give its rows of full attention; under contiguous
+    causal masking the pairs j > i are empty (lse -inf)."""
+    rng = np.random.default_rng(21)
+    S, N, D = 30, 5, 6
+    q, k, v = (_rand(rng, S, D, scale=2.0) for _ in range(3))
+    c = S // N
+    full_o, full_l = orc.attention_rows(q, k, v, np.arange(S), N, causal, layout)
+    for i in range(N):
+        o = np.zeros((c, D))
+        lse = np.full(c, -np.inf)
+        for j in orc.ring_order(i, N):
+            oj, lj = orc.block_pair_attention(q, k, v, i, j, N, causal, layout)
+            if causal and layout == "contiguous" and j > i:
+                assert np.all(lj == -np.inf) and np.all(oj == 0)
+            o, lse = orc.lse_merge(o, lse, oj, lj)
+        np.testing.assert_allclose(o, full_o[i * c:(i + 1) * c], atol=1e-13)
+        np.testing.assert_allclose(lse, full_l[i * c:(i + 1) * c], atol=1e-13)
+
+
 def test_merge_edge_cases():
     o = np.arange(6.0).reshape(2, 3)
     ninf = np.array([-np.inf, -np.inf])

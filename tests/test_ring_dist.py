@@ -1,0 +1,102 @@
+"""Multi-process ring forward on CPU (gloo): the K/V exchange protocol of
+ring_attention_fwd_gb300.ring with the CPU oracle computing each block pair.
+
+Each rank is one ring host.  The injected block compute checks that the K/V
+block a rank holds in round s is exactly block (rank - s) mod N, then folds
+the oracle's partial state for that pair; the final rows of every rank must
+equal the oracle's full attention.  No GPU is involved."""
+import datetime
+import os
+import socket
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import oracle as orc
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _inputs(S, D, seed):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((S, D)) for _ in range(3)]
+
+
+def _worker(rank, world, port, S, D, causal, layout, outdir, mode):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=20))
+    try:
+        from ring_attention_fwd_gb300.ring import ring_forward
+        q, k, v = _inputs(S, D, 5)
+        c = S // world
+        blk = lambda x, b: torch.from_numpy(x[b * c:(b + 1) * c].copy())[None, None]  # [1,1,c,D]
+        seen = []
+
+        def step(qq, kk, vv, n, i, j):
+            assert torch.equal(kk, blk(k, j)) and torch.equal(vv, blk(v, j)), f"rank {i}: wrong block for {j}"
+            seen.append(j)
+            qf, kf, vf = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+            qf[i * c:(i + 1) * c] = qq[0, 0].numpy()
+            kf[j * c:(j + 1) * c] = kk[0, 0].numpy()
+            vf[j * c:(j + 1) * c] = vv[0, 0].numpy()
+            o, l = orc.block_pair_attention(qf, kf, vf, i, j, n, causal, layout)
+            return torch.from_numpy(o)[None, None], torch.from_numpy(l)[None, None]
+
+        def merge(o, l, oj, lj):
+            mo, ml = orc.lse_merge(o[0, 0].numpy(), l[0, 0].numpy(), oj[0, 0].numpy(), lj[0, 0].numpy())
+            o[0, 0] = torch.from_numpy(mo)
+            l[0, 0] = torch.from_numpy(ml)
+
+        if mode == "leave" and rank == 1:
+            return                       # this host leaves before its first send
+        try:
+            o, l = ring_forward(blk(q, rank), blk(k, rank), blk(v, rank), causal=causal, layout=layout,
+                                step=step, merge=merge, timeout_s=3.0 if mode == "leave" else None)
+        except Exception as e:           # noqa: BLE001 - reported to the parent
+            with open(os.path.join(outdir, f"err{rank}.txt"), "w") as f:
+                f.write(type(e).__name__ + ": " + str(e))
+            return
+        np.save(os.path.join(outdir, f"o{rank}.npy"), o[0, 0].numpy())
+        np.save(os.path.join(outdir, f"l{rank}.npy"), l[0, 0].numpy())
+        np.save(os.path.join(outdir, f"seen{rank}.npy"), np.array(seen))
+    finally:
+        if mode != "leave":
+            dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,layout,causal", [(2, "contiguous", True), (2, "striped", True),
+                                                 (4, "striped", True), (4, "contiguous", True),
+                                                 (3, "contiguous", False)])
+def test_ring_forward_gloo_matches_full_attention(world, layout, causal):
+    S, D = 12 * world, 8
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_worker, args=(world, _free_port(), S, D, causal, layout, d, "ok"), nprocs=world, join=True)
+        q, k, v = _inputs(S, D, 5)
+        c = S // world
+        fo, fl = orc.attention_rows(q, k, v, np.arange(S), world, causal, layout)
+        for r in range(world):
+            assert not os.path.exists(os.path.join(d, f"err{r}.txt")), open(os.path.join(d, f"err{r}.txt")).read()
+            np.testing.assert_allclose(np.load(os.path.join(d, f"o{r}.npy")), fo[r * c:(r + 1) * c], atol=1e-12)
+            np.testing.assert_allclose(np.load(os.path.join(d, f"l{r}.npy")), fl[r * c:(r + 1) * c], atol=1e-12)
+            order = orc.ring_order(r, world)
+            expect = [j for j in order if not (causal and layout == "contiguous" and j > r)]
+            assert np.load(os.path.join(d, f"seen{r}.npy")).tolist() == expect
+
+
+@pytest.mark.timeout(120)
+def test_ring_forward_reports_a_host_that_left():
+    """A host that leaves before sending must surface as an error on its
+    neighbour within the exchange time-out, not as a hang."""
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_worker, args=(2, _free_port(), 24, 8, True, "striped", d, "leave"), nprocs=2, join=True)
+        assert os.path.exists(os.path.join(d, "err0.txt"))
+        assert not os.path.exists(os.path.join(d, "o0.npy"))
