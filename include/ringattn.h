@@ -233,6 +233,18 @@ RA_API int ra_set_kernel_timing(int enable);
 RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
 
 /*
+ * ra_set_wait_test -- test aid for the bounded waits (no counterpart on the
+ * pages).  ra_set_wait_test(1) makes the NEXT bf16 ra_fwd call (from any
+ * thread) withhold the first query tile of every CTA, so no data for it ever
+ * arrives: the kernel's waits run out after their 2-second limit, each CTA
+ * abandons its work, releases its resources and returns, and the following
+ * ra_check_device_status() returns RA_ERR_TIMEOUT.  That call's outputs are
+ * unspecified; the device and the library stay usable.  The switch clears
+ * itself once used; ra_set_wait_test(0) clears it unused.
+ */
+RA_API int ra_set_wait_test(int enable);
+
+/*
  * ra_check_device_status -- synchronise `stream`, then read and clear the
  * library's device-side status word.  Returns RA_ERR_TIMEOUT if any kernel
  * launched since the previous check gave up a bounded wait (the kernel then

@@ -38,6 +38,7 @@ SIGNATURES = {
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
     "ra_set_kernel_timing": (_int, [_int]),
+    "ra_set_wait_test": (_int, [_int]),
     "ra_kernel_times": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_int)]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),

@@ -140,6 +140,7 @@ struct FwdArgs {
   int64_t B, H, S, D, N;
   int causal, striped;
   int strict;                  // see RingGeom::strict (0 for whole-sequence calls)
+  int withhold_first_q;        // test aid, bf16 kernel: see ra_set_wait_test
   unsigned int* status;
   unsigned long long* timing;  // [N*N] or null
   cudaStream_t stream;

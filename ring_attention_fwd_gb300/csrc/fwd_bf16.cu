@@ -68,6 +68,7 @@ struct Params {
   float* LSE;
   unsigned int* status;
   unsigned long long* timing;      // [N*N] ns accumulators or null
+  int withhold_first_q;            // test aid: never load the first unit's Q (waits then time out)
 };
 
 // K-major operand tile (rows x 128 cols bf16, two 128B-swizzled 64-col boxes):
@@ -140,12 +141,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (!(ok = mbar_wait(&bars->q_empty, qe_ph, wc, ST_FWD_WAIT | 1))) break;
           qe_ph ^= 1;
         }
-        mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
-        const int qrow = w.i * g.c + w.r0;
-        for (int q = 0; q < 2; ++q)
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(smem + OFF_Q + q * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full, h * 64,
-                        qrow + q * BM, w.bh);
+        if (!(p.withhold_first_q && nq == 0)) {
+          mbar_arrive_expect_tx(&bars->q_full, 2 * TILE_BYTES);
+          const int qrow = w.i * g.c + w.r0;
+          for (int q = 0; q < 2; ++q)
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + OFF_Q + q * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full, h * 64,
+                          qrow + q * BM, w.bh);
+        }
         ++nq;
         for (int s = 0; s < g.N && ok; ++s) {
           const int j = ring_block(w.i, s, g.N);
@@ -404,6 +407,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   p.LSE = a.LSE;
   p.status = a.status;
   p.timing = a.timing;
+  p.withhold_first_q = a.withhold_first_q;
   static bool attr_done = false;  // benign race: idempotent attribute set
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

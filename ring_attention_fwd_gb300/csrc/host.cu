@@ -73,6 +73,7 @@ int device_state(DevState** out) {
   return RA_OK;
 }
 
+std::atomic<int> g_wait_test{0};   // one-shot: next bf16 forward withholds its first Q tile
 std::atomic<uint64_t*> g_timing_buf{nullptr};
 std::atomic<size_t> g_timing_n{0};
 
@@ -199,6 +200,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
   a.causal = causal;
   a.striped = layout == RA_STRIPED;
   a.strict = strict;
+  a.withhold_first_q = dtype == RA_BF16 ? g_wait_test.exchange(0) : 0;
   a.status = d->status;
   a.timing = reinterpret_cast<unsigned long long*>(timing);
   a.stream = static_cast<cudaStream_t>(stream);
@@ -234,6 +236,12 @@ int ra_set_timing_buffer(uint64_t* dev_buf, size_t n) {
   if (dev_buf != nullptr && n < 1) return fail(RA_ERR_ARG, "timing buffer of size 0");
   g_timing_n.store(dev_buf ? n : 0);
   g_timing_buf.store(dev_buf);
+  return RA_OK;
+}
+
+int ra_set_wait_test(int enable) {
+  if (enable != 0 && enable != 1) return fail(RA_ERR_ARG, "ra_set_wait_test: enable must be 0 or 1");
+  g_wait_test.store(enable);
   return RA_OK;
 }
 

@@ -27,7 +27,7 @@ def declared_symbols():
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
-        "ra_set_kernel_timing", "ra_kernel_times", "ra_check_device_status", "ra_last_error", "ra_version"])
+        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -123,6 +123,11 @@ def test_fwd_step_rejects_bad_block_indices(L):
     assert call(4, 0, -1) == 1
     assert call(0, 0, 0) == 1
     assert L.ra_fwd_step(None, FAKE, FAKE, 1, 1, 64, 128, 4, 1, 0, 1, 0, 1, FAKE, FAKE, None) == 1
+
+
+def test_wait_test_switch_arguments(L):
+    assert L.ra_set_wait_test(3) == 1
+    assert L.ra_set_wait_test(0) == 0
 
 
 def test_kernel_timing_arguments(L):
