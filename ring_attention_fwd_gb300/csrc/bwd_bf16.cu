@@ -22,9 +22,12 @@
 //                   over dP^T in TMEM; dV += P^T dO and dK += dS^T Q read them
 //                   from there.
 //   3. dq_kernel    Query-stationary, visiting KV tiles in the forward's ring
-//                   order; Q and dO sit in TMEM as A operands.  Per KV tile:
-//                   S = Q K^T, dP = dO V^T; dS (bf16) packed over dP in TMEM;
-//                   dQ += dS K with dQ accumulating in TMEM.
+//                   order; Q sits in TMEM as an A operand, dO in shared
+//                   memory.  Per KV tile: S = Q K^T, dP = dO V^T; P is taken
+//                   from S while dP is still being computed; dS (bf16) goes to
+//                   its own TMEM region; dQ += dS K accumulates in TMEM.  S
+//                   and dP are released as soon as they are in registers, so
+//                   the next tile's S and dP MMAs overlap this tile's work.
 // Every MMA is 128 wide (an MMA instruction costs ~93 clocks at any size on
 // this part, so wide ones keep the tensor pipe fed).  Overlap: the elementwise
 // warps release S as soon as it is in registers, so the next tile's S MMA runs
@@ -107,26 +110,6 @@ struct Params {
 
 __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int qt) {
   return ((static_cast<int64_t>(bh) * g.N + i) * g.n_mb + qt) * BT;
-}
-
-// Copies one 128-element bf16 row from global memory into 64 TMEM columns of
-// this thread's lane (element pairs packed low-first, the layout of a K-major
-// A operand), or zeros when the row lies past the end of the tensor.
-__device__ __forceinline__ void row_to_tmem(const __nv_bfloat16* src, uint32_t tcol, bool in_bounds) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t v[32];
-    const uint4* s4 = reinterpret_cast<const uint4*>(src) + half * 8;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 x = in_bounds ? __ldg(s4 + k) : make_uint4(0u, 0u, 0u, 0u);
-      v[4 * k] = x.x;
-      v[4 * k + 1] = x.y;
-      v[4 * k + 2] = x.z;
-      v[4 * k + 3] = x.w;
-    }
-    tmem_st32(tcol + half * 32, v);
-  }
 }
 
 // ============================================================== dK, dV
@@ -453,24 +436,27 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 // ============================================================== dQ
 namespace q {
 constexpr int KSTAGE = 3;
-constexpr uint32_t OFF_K = 0;                               // KSTAGE tiles
+constexpr uint32_t OFF_DO = 0;                              // dO tile of the unit
+constexpr uint32_t OFF_K = OFF_DO + TILE_BYTES;             // KSTAGE tiles
 constexpr uint32_t OFF_V = OFF_K + KSTAGE * TILE_BYTES;     // KSTAGE tiles
 constexpr uint32_t OFF_BAR = OFF_V + KSTAGE * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Bars {
+  uint64_t do_full, do_empty;
   uint64_t k_full[KSTAGE], v_full[KSTAGE], kv_empty[KSTAGE];
-  uint64_t qo_full, qo_empty, s_full, s_free, p_full, dq_full, dq_empty, drain;
+  uint64_t qo_full, qo_empty, s_full, s_free, dp_full, dp_free, p_full, ds_free, dq_full, dq_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
-// Packed bf16 column of the 16-key K-slice kk of dS inside the dP region:
-// warpgroup g (keys [64g, 64g+64)) packs its dS at [64g, 64g+32).
-__device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
+// Packed bf16 column of the 16-key K-slice kk of dS inside the dS region:
+// warpgroup g (keys [64g, 64g+64)) packs its dS at [32g, 32g+32).
+__device__ __forceinline__ uint32_t pcol(int kk) { return 32 * (kk >> 2) + 8 * (kk & 3); }
 
 __global__ void __launch_bounds__(THREADS, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-          const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ dO, const Params p) {
+          const __grid_constant__ CUtensorMap tmDO, const __nv_bfloat16* __restrict__ Q, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
   const uint32_t sbase = smem_u32(smem);
@@ -482,6 +468,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     return;
   }
   if (threadIdx.x == 0) {
+    mbar_init(&bars->do_full, 1);
+    mbar_init(&bars->do_empty, 1);
     for (int s = 0; s < KSTAGE; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -491,7 +479,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     mbar_init(&bars->qo_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 256);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 256);
     mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_empty, 256);
     mbar_init(&bars->drain, 1);
@@ -506,9 +497,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // TMEM: dQ [0,128) Q [128,192) dO [192,256) (bf16 rows, A operands)
-  //       S [256,384) dP [384,512); dS is packed (bf16) over dP once read.
-  const uint32_t T_DQ = tmem, T_Q = tmem + 128, T_DO = tmem + 192, T_S = tmem + 256, T_DP = tmem + 384;
+  // TMEM: dQ [0,128) Q [128,192) (bf16 rows, A operand) dS [192,256) (bf16, A operand)
+  //       S [256,384) dP [384,512).  S and dP are free again as soon as they are
+  //       in registers, so the next KV tile's S and dP MMAs overlap this tile's
+  //       elementwise work.
+  const uint32_t T_DQ = tmem, T_Q = tmem + 128, T_DS = tmem + 192, T_S = tmem + 256, T_DP = tmem + 384;
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int grid = gridDim.x, cta = blockIdx.x;
 
@@ -517,12 +510,21 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       // ------------------------------------------------------------ producer
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t it = 0;
+      tma_prefetch_desc(&tmDO);
+      uint32_t it = 0, nd = 0, de_ph = 0;
       bool ok = true;
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
+        if (nd > 0) {
+          if (!(ok = mbar_wait(&bars->do_empty, de_ph, wc, ST_BWD_WAIT | 0x11))) break;
+          de_ph ^= 1;
+        }
+        mbar_arrive_expect_tx(&bars->do_full, TILE_BYTES);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(smem + OFF_DO + h * BOX_BYTES, &tmDO, &bars->do_full, h * 64, w.i * g.c + w.r0, w.bh);
+        ++nd;
         for (int s = 0; s < g.N && ok; ++s) {
           const int j = ring_block(w.i, s, g.N);
           if (!block_visited(g, w.i, j)) continue;
@@ -540,28 +542,31 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           }
         }
       }
-      if (!ok)
+      if (!ok) {
         for (uint32_t k = (it > KSTAGE ? it - KSTAGE : 0); k < it; ++k) {
           mbar_drain(&bars->k_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
           mbar_drain(&bars->v_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
         }
+        if (nd > 0) mbar_drain(&bars->do_full, (nd - 1) & 1, 200000000ull);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A (TMEM), B K-major, N = 128
+      constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // B K-major, N = 128
       constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A (TMEM), B MN-major
-      uint32_t it = 0, qo_ph = 0, sf_ph = 0, pf_ph = 0, dqe_ph = 0;
-      bool ok = true, first_unit = true, first_s = true;
-      auto issue_s = [=](int st) {   // S = Q K^T
+      const uint64_t dDO0 = kdesc0(sbase + OFF_DO);
+      uint32_t it = 0, de_ph = 0, qo_ph = 0, sf_ph = 0, df_ph = 0, pf_ph = 0, dqe_ph = 0;
+      bool ok = true, first_unit = true, first_s = true, first_dp = true;
+      auto issue_s = [=](int st) {   // S = Q K^T  (Q from TMEM)
         const uint64_t bk = kdesc0(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ts(T_S, T_Q + kk * 8, kslice(bk, kk), ID_KK, kk > 0);
       };
-      auto issue_dp = [=](int st) {  // dP = dO V^T
+      auto issue_dp = [=](int st) {  // dP = dO V^T  (dO from shared memory)
         const uint64_t bv = kdesc0(sbase + OFF_V + st * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ts(T_DP, T_DO + kk * 8, kslice(bv, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kslice(dDO0, kk), kslice(bv, kk), ID_KK, kk > 0);
       };
       auto wait_kv = [&](uint32_t k_it) -> bool {
         const int st = k_it % KSTAGE;
@@ -570,33 +575,41 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         if (!mbar_wait(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15)) return false;
         return true;
       };
+      // S for KV tile k_it once the previous S is in registers, then dP once the
+      // previous dP is in registers.
+      auto issue_tile = [&](uint32_t k_it) -> bool {
+        if (!wait_kv(k_it)) return false;
+        if (!first_s) {
+          if (!mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c)) return false;
+          sf_ph ^= 1;
+        }
+        first_s = false;
+        tc_fence_after();
+        issue_s(k_it % KSTAGE);
+        mma_commit(&bars->s_full);
+        if (!first_dp) {
+          if (!mbar_wait(&bars->dp_free, df_ph, wc, ST_BWD_WAIT | 0x1d)) return false;
+          df_ph ^= 1;
+        }
+        first_dp = false;
+        tc_fence_after();
+        issue_dp(k_it % KSTAGE);
+        mma_commit(&bars->dp_full);
+        return true;
+      };
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
         const int T = unit_tiles(g, w.i, w.r0);
-        if (!(ok = mbar_wait(&bars->qo_full, qo_ph, wc, ST_BWD_WAIT | 0x13))) break;
+        if (!(ok = mbar_wait(&bars->do_full, de_ph, wc, ST_BWD_WAIT | 0x13))) break;
+        de_ph ^= 1;
+        if (!(ok = mbar_wait(&bars->qo_full, qo_ph, wc, ST_BWD_WAIT | 0x1e))) break;
         qo_ph ^= 1;
-        if (!(ok = wait_kv(it))) break;
-        if (!first_s) {   // S region: the previous tile's S must have been read
-          if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c))) break;
-          sf_ph ^= 1;
-        }
-        first_s = false;
-        tc_fence_after();
-        issue_s(it % KSTAGE);
-        issue_dp(it % KSTAGE);   // dP region: last read by the previous tile's dQ MMAs
-        mma_commit(&bars->s_full);
+        if (!(ok = issue_tile(it))) break;
         for (int t = 0; t < T && ok; ++t, ++it) {
           const int st = it % KSTAGE;
-          const int nst = (it + 1) % KSTAGE;
-          if (t + 1 < T) {   // next tile's S as soon as this tile's S is in registers
-            if (!(ok = wait_kv(it + 1))) break;
-            if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c))) break;
-            sf_ph ^= 1;
-            tc_fence_after();
-            issue_s(nst);
-          }
+          if (t + 1 < T && !(ok = issue_tile(it + 1))) break;
           if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 0x16))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
@@ -606,13 +619,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           tc_fence_after();
           const uint64_t mk = mndesc0(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS packed in TMEM, K MN-major)
-            mma_ts(T_DQ, T_DP + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
+          for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS from TMEM, K MN-major)
+            mma_ts(T_DQ, T_DS + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
+          mma_commit(&bars->ds_free);
           mma_commit(&bars->kv_empty[st]);
-          if (t + 1 < T) {
-            issue_dp(nst);
-            mma_commit(&bars->s_full);
-          } else {
+          if (t == T - 1) {
+            mma_commit(&bars->do_empty);
             mma_commit(&bars->qo_empty);
             mma_commit(&bars->dq_full);
           }
@@ -623,29 +635,42 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else if (warp >= 4) {
-    // ----------------------------------------- Q/dO rows, dS, epilogue
+    // ------------------------------------------------- Q rows, dS, epilogue
     const int grp = (warp - 4) >> 2;                     // key columns [64*grp, +64)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                    // query row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t s_ph = 0, dq_ph = 0, qoe_ph = 0;
-    bool ok = true, first_unit = true;
+    uint32_t s_ph = 0, dp_ph = 0, dsf_ph = 0, dq_ph = 0, qoe_ph = 0;
+    bool ok = true, first_unit = true, first_ds = true;
     for (int64_t r = 0; ok; ++r) {
       const int64_t u = snake_pos(r, cta, grid);
       if (u >= p.num_units) break;
       const Unit w = unit_at(g, u);
       const int rq = w.r0 + row;
       const int64_t grow = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
-      // ---- this unit's Q (group 0) or dO (group 1) row into TMEM
+      // ---- this unit's Q row into TMEM: group g copies head-dim columns [64g, 64g+64)
       if (!first_unit) {
         if (!(ok = mbar_wait(&bars->qo_empty, qoe_ph, wc, ST_BWD_WAIT | 0x1b))) break;
         qoe_ph ^= 1;
         tc_fence_after();
       }
       first_unit = false;
-      row_to_tmem((grp == 0 ? Q : dO) + grow * HD, (grp == 0 ? T_Q : T_DO) + lane_off, w.i * g.c + rq < p.S);
-      tmem_st_wait();
+      {
+        uint32_t v[32];
+        const uint4* s4 = reinterpret_cast<const uint4*>(Q + grow * HD + 64 * grp);
+        const bool inb = w.i * g.c + rq < p.S;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 x = inb ? __ldg(s4 + k) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * k] = x.x;
+          v[4 * k + 1] = x.y;
+          v[4 * k + 2] = x.z;
+          v[4 * k + 3] = x.w;
+        }
+        tmem_st32(T_Q + lane_off + 32 * grp, v);
+        tmem_st_wait();
+      }
       tc_fence_before();
       mbar_arrive(&bars->qo_full);
       const int64_t vr = vec_row(g, w.bh, w.i, w.r0 / BT) + row;
@@ -657,38 +682,45 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         const int last = kt_last(g, w.i, j, w.r0);
         const int lim = key_limit(g, w.i, j, rq);
         for (int kt = 0; kt <= last && ok; ++kt) {
+          // P from S as soon as S is ready (the dP MMA may still be running)
           if (!(ok = mbar_wait(&bars->s_full, s_ph, wc, ST_BWD_WAIT | 0x18))) break;
           s_ph ^= 1;
           tc_fence_after();
-          const uint32_t tS = T_S + lane_off + 64 * grp;
-          const uint32_t tDP = T_DP + lane_off + 64 * grp;
-          uint32_t sv[64], dpv[64];
-          tmem_ld32(tS, sv);
-          tmem_ld32(tS + 32, sv + 32);
-          tmem_ld32(tDP, dpv);
-          tmem_ld32(tDP + 32, dpv + 32);
+          uint32_t pv[64];
+          tmem_ld32(T_S + lane_off + 64 * grp, pv);
+          tmem_ld32(T_S + lane_off + 64 * grp + 32, pv + 32);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bars->s_free);
           const bool masked = tile_masked(g, w.i, j, kt, w.r0);
-          const int rk0 = kt * BT + 64 * grp;               // first key row handled here
+          const int rk0 = kt * BT + 64 * grp;                // first key row handled here
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t dk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const int c = hh * 32 + k;
-              float p0 = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2_r));
-              float p1 = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2_r));
-              if (masked) {
-                if (rk0 + c >= lim) p0 = 0.f;
-                if (rk0 + c + 1 >= lim) p1 = 0.f;
-              }
-              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[c]) - dvec_r),
-                                       p1 * (__uint_as_float(dpv[c + 1]) - dvec_r));
-            }
-            tmem_st16(tDP + hh * 16, dk);   // dS over this group's own dP columns
+          for (int c = 0; c < 64; ++c) {
+            float pc = hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r));
+            if (masked && rk0 + c >= lim) pc = 0.f;
+            pv[c] = __float_as_uint(pc);
           }
+          if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0x1f))) break;
+          dp_ph ^= 1;
+          tc_fence_after();
+          uint32_t dpv[64];
+          tmem_ld32(T_DP + lane_off + 64 * grp, dpv);
+          tmem_ld32(T_DP + lane_off + 64 * grp + 32, dpv + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->dp_free);
+          uint32_t dk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2)
+            dk[c >> 1] = pack_bf16x2(__uint_as_float(pv[c]) * (__uint_as_float(dpv[c]) - dvec_r),
+                                     __uint_as_float(pv[c + 1]) * (__uint_as_float(dpv[c + 1]) - dvec_r));
+          if (!first_ds) {   // the dS region: the previous tile's dQ MMAs must have read it
+            if (!(ok = mbar_wait(&bars->ds_free, dsf_ph, wc, ST_BWD_WAIT | 0x20))) break;
+            dsf_ph ^= 1;
+            tc_fence_after();
+          }
+          first_ds = false;
+          tmem_st32(T_DS + lane_off + 32 * grp, dk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&bars->p_full);
@@ -808,8 +840,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   kv::dkv_kernel<<<grid, THREADS, kv::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev) cudaEventRecord(a.ev[2], a.stream);
-  q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.Q),
-                                                           static_cast<const __nv_bfloat16*>(a.dO), p);
+  q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mk, mv, mdo, static_cast<const __nv_bfloat16*>(a.Q), p);
   e = cudaGetLastError();
   if (a.ev) cudaEventRecord(a.ev[3], a.stream);
   return e;
