@@ -114,19 +114,27 @@ __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int
 
 // ============================================================== dK, dV
 namespace kv {
-constexpr int QSTAGE = 2;
+// Q tiles (with their lse2 rows) and dO tiles (with their D_vec rows) stream
+// through separate rings.  Q is the first operand a tile needs (S^T) and the
+// last one it releases (dK), so it gets the deeper ring; dO is released after
+// dV, a tile earlier.
+constexpr int QSTAGE = 3;
+constexpr int DSTAGE = 2;
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
-constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;              // QSTAGE tiles
-constexpr uint32_t OFF_DO = OFF_Q + QSTAGE * TILE_BYTES;    // QSTAGE tiles
-constexpr uint32_t OFF_VEC = OFF_DO + QSTAGE * TILE_BYTES;  // QSTAGE x (lse2[128], dvec[128])
-constexpr uint32_t OFF_BAR = OFF_VEC + QSTAGE * 2 * VEC_BYTES;
+constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;               // QSTAGE tiles
+constexpr uint32_t OFF_DO = OFF_Q + QSTAGE * TILE_BYTES;     // DSTAGE tiles
+constexpr uint32_t OFF_LSE = OFF_DO + DSTAGE * TILE_BYTES;   // QSTAGE x lse2[128]
+constexpr uint32_t OFF_DVEC = OFF_LSE + QSTAGE * VEC_BYTES;  // DSTAGE x dvec[128]
+constexpr uint32_t OFF_BAR = OFF_DVEC + DSTAGE * VEC_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Bars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[QSTAGE], q_empty[QSTAGE];
-  uint64_t s_full, s_free, p_full, dkv_full, dkv_empty, drain;
+  uint64_t do_full[DSTAGE], do_empty[DSTAGE];
+  uint64_t s_full, s_free, dp_full, p_full, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -187,8 +195,13 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
     }
+    for (int s = 0; s < DSTAGE; ++s) {
+      mbar_init(&bars->do_full[s], 1);
+      mbar_init(&bars->do_empty[s], 1);
+    }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 256);
+    mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 256);
@@ -217,7 +230,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      uint32_t it = 0, nkv = 0, kve_ph = 0;
+      uint32_t nq = 0, ndo = 0, nkv = 0, kve_ph = 0;
       bool ok = true;
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
@@ -238,25 +251,32 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int s = 0; s < g.N && ok; ++s) {
           const int i = (j + s) % g.N;
           if (!q_block_visited(g, i, j)) continue;
-          for (int qt = qt_first(g, i, j, kt); qt < g.n_mb; ++qt, ++it) {
-            const int st = it % QSTAGE;
-            if (!(ok = mbar_wait(&bars->q_empty[st], ((it / QSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 2))) break;
-            mbar_arrive_expect_tx(&bars->q_full[st], 2 * TILE_BYTES + 2 * VEC_BYTES);
+          for (int qt = qt_first(g, i, j, kt); qt < g.n_mb; ++qt) {
             const int qrow = i * g.c + qt * BT;
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(smem + OFF_Q + st * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full[st], h * 64, qrow, bh);
-              tma_load_3d(smem + OFF_DO + st * TILE_BYTES + h * BOX_BYTES, &tmDO, &bars->q_full[st], h * 64, qrow,
-                          bh);
-            }
             const int64_t vrow = vec_row(g, bh, i, qt);
-            bulk_load(smem + OFF_VEC + st * 2 * VEC_BYTES, p.lse2 + vrow, VEC_BYTES, &bars->q_full[st]);
-            bulk_load(smem + OFF_VEC + st * 2 * VEC_BYTES + VEC_BYTES, p.dvec + vrow, VEC_BYTES, &bars->q_full[st]);
+            const int sq = nq % QSTAGE;
+            if (!(ok = mbar_wait(&bars->q_empty[sq], ((nq / QSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 2))) break;
+            mbar_arrive_expect_tx(&bars->q_full[sq], TILE_BYTES + VEC_BYTES);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + OFF_Q + sq * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full[sq], h * 64, qrow, bh);
+            bulk_load(smem + OFF_LSE + sq * VEC_BYTES, p.lse2 + vrow, VEC_BYTES, &bars->q_full[sq]);
+            ++nq;
+            const int sd = ndo % DSTAGE;
+            if (!(ok = mbar_wait(&bars->do_empty[sd], ((ndo / DSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0xb))) break;
+            mbar_arrive_expect_tx(&bars->do_full[sd], TILE_BYTES + VEC_BYTES);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(smem + OFF_DO + sd * TILE_BYTES + h * BOX_BYTES, &tmDO, &bars->do_full[sd], h * 64, qrow,
+                          bh);
+            bulk_load(smem + OFF_DVEC + sd * VEC_BYTES, p.dvec + vrow, VEC_BYTES, &bars->do_full[sd]);
+            ++ndo;
           }
         }
       }
       if (!ok) {
-        for (uint32_t k = (it > QSTAGE ? it - QSTAGE : 0); k < it; ++k)
+        for (uint32_t k = (nq > QSTAGE ? nq - QSTAGE : 0); k < nq; ++k)
           mbar_drain(&bars->q_full[k % QSTAGE], (k / QSTAGE) & 1, 200000000ull);
+        for (uint32_t k = (ndo > DSTAGE ? ndo - DSTAGE : 0); k < ndo; ++k)
+          mbar_drain(&bars->do_full[k % DSTAGE], (k / DSTAGE) & 1, 200000000ull);
         if (nkv > 0) mbar_drain(&bars->kv_full, (nkv - 1) & 1, 200000000ull);
       }
     }
@@ -273,8 +293,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_S, kslice(dK0, kk), kslice(bq, kk), ID_KK, kk > 0);
       };
-      auto issue_dp = [=](int st) {  // dP^T = V dO^T
-        const uint64_t bdo = kdesc0(sbase + OFF_DO + st * TILE_BYTES);
+      auto issue_dp = [=](int sd) {  // dP^T = V dO^T
+        const uint64_t bdo = kdesc0(sbase + OFF_DO + sd * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kslice(dV0, kk), kslice(bdo, kk), ID_KK, kk > 0);
       };
@@ -294,17 +314,21 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         first_s = false;
         tc_fence_after();
         issue_s(it % QSTAGE);
-        issue_dp(it % QSTAGE);   // dP^T region: last read by the previous tile's dV / dK MMAs
         mma_commit(&bars->s_full);
+        if (!(ok = mbar_wait(&bars->do_full[it % DSTAGE], (it / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
+        tc_fence_after();
+        issue_dp(it % DSTAGE);   // dP^T region: last read by the previous tile's dV / dK MMAs
+        mma_commit(&bars->dp_full);
         for (int t = 0; t < T && ok; ++t, ++it) {
-          const int st = it % QSTAGE;
-          const int nst = (it + 1) % QSTAGE;
+          const int st = it % QSTAGE, sd = it % DSTAGE;
+          const int nst = (it + 1) % QSTAGE, nsd = (it + 1) % DSTAGE;
           if (t + 1 < T) {   // next tile's S^T as soon as this tile's S^T is in registers
             if (!(ok = mbar_wait(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
             if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
             sf_ph ^= 1;
             tc_fence_after();
             issue_s(nst);
+            mma_commit(&bars->s_full);
           }
           if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 5))) break;
           pf_ph ^= 1;
@@ -314,17 +338,20 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           }
           tc_fence_after();
           const uint32_t acc = t > 0 ? 1u : 0u;
-          const uint64_t mdo = mndesc0(sbase + OFF_DO + st * TILE_BYTES), mq = mndesc0(sbase + OFF_Q + st * TILE_BYTES);
+          const uint64_t mdo = mndesc0(sbase + OFF_DO + sd * TILE_BYTES), mq = mndesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO
             mma_ts(T_DV, T_DP + pcol_p(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
+          mma_commit(&bars->do_empty[sd]);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q
             mma_ts(T_DK, T_DP + pcol_ds(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
           mma_commit(&bars->q_empty[st]);
           if (t + 1 < T) {
-            issue_dp(nst);
-            mma_commit(&bars->s_full);
+            if (!(ok = mbar_wait(&bars->do_full[nsd], ((it + 1) / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
+            tc_fence_after();
+            issue_dp(nsd);
+            mma_commit(&bars->dp_full);
           }
         }
         if (!ok) break;
@@ -342,7 +369,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int t_row = quad * 32 + lane;                  // key row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t it = 0, s_ph = 0, dkv_ph = 0;
+    uint32_t it = 0, s_ph = 0, dp_ph = 0, dkv_ph = 0;
     bool ok = true;
     for (int64_t r = 0; ok; ++r) {
       const int64_t u = snake_pos(r, cta, grid);
@@ -357,49 +384,54 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const bool dpair = diag_type(g, i, j);
         const int incl = diag_incl(g, i, j);
         for (int qt = qt_first(g, i, j, kt); qt < g.n_mb && ok; ++qt, ++it) {
-          const int st = it % QSTAGE;
+          const int st = it % QSTAGE, sd = it % DSTAGE;
           if (!(ok = mbar_wait(&bars->q_full[st], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 7))) break;
+          if (!(ok = mbar_wait(&bars->do_full[sd], (it / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xe))) break;
           if (!(ok = mbar_wait(&bars->s_full, s_ph, wc, ST_BWD_WAIT | 8))) break;
           s_ph ^= 1;
           tc_fence_after();
           const uint32_t tS = T_S + lane_off + 64 * grp;
           const uint32_t tDP = T_DP + lane_off + 64 * grp;
-          uint32_t sv[64], dpv[64];
+          uint32_t sv[64];
           tmem_ld32(tS, sv);
           tmem_ld32(tS + 32, sv + 32);
-          tmem_ld32(tDP, dpv);
-          tmem_ld32(tDP + 32, dpv + 32);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bars->s_free);
-          // query column q of the tile is visible to this key row iff q >= vis_lo
+          // P^T while the previous tile's dV / dK and this tile's dP^T run.
+          // Query column q of the tile is visible to this key row iff q >= vis_lo.
           int vis_lo = 0;
           if (!key_ok) vis_lo = BT;
           else if (dpair && qt == kt) vis_lo = t_row + 1 - incl;
-          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_VEC + st * 2 * VEC_BYTES) + 64 * grp;
-          const float* dvec = lse2 + BT;
+          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_LSE + st * VEC_BYTES) + 64 * grp;
+          const float* dvec = reinterpret_cast<const float*>(smem + OFF_DVEC + sd * VEC_BYTES) + 64 * grp;
           const int q0 = 64 * grp;
+          float pv[64];
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+            pv[c] = q0 + c < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+            pv[c + 1] = q0 + c + 1 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+            pv[c + 2] = q0 + c + 2 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+            pv[c + 3] = q0 + c + 3 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+          }
+          if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0xf))) break;
+          dp_ph ^= 1;
+          tc_fence_after();
+          uint32_t dpv[64];
+          tmem_ld32(tDP, dpv);
+          tmem_ld32(tDP + 32, dpv + 32);
+          tmem_ld_wait();
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int k = 0; k < 32; k += 4) {
+            for (int k = 0; k < 32; k += 2) {
               const int c = hh * 32 + k;
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-              const float4 d4 = *reinterpret_cast<const float4*>(dvec + c);
-              float p0 = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-              float p1 = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-              float p2 = hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-              float p3 = hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
-              if (q0 + c < vis_lo) p0 = 0.f;
-              if (q0 + c + 1 < vis_lo) p1 = 0.f;
-              if (q0 + c + 2 < vis_lo) p2 = 0.f;
-              if (q0 + c + 3 < vis_lo) p3 = 0.f;
-              pk[k >> 1] = pack_bf16x2(p0, p1);
-              pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
-              dk[k >> 1] = pack_bf16x2(p0 * (__uint_as_float(dpv[c]) - d4.x), p1 * (__uint_as_float(dpv[c + 1]) - d4.y));
-              dk[(k >> 1) + 1] =
-                  pack_bf16x2(p2 * (__uint_as_float(dpv[c + 2]) - d4.z), p3 * (__uint_as_float(dpv[c + 3]) - d4.w));
+              const float2 d2 = *reinterpret_cast<const float2*>(dvec + c);
+              pk[k >> 1] = pack_bf16x2(pv[c], pv[c + 1]);
+              dk[k >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[c]) - d2.x),
+                                       pv[c + 1] * (__uint_as_float(dpv[c + 1]) - d2.y));
             }
             tmem_st16(tDP + hh * 16, pk);        // P^T over this group's own dP^T columns
             tmem_st16(tDP + 32 + hh * 16, dk);   // dS^T
