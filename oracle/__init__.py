@@ -5,3 +5,4 @@ from .attention import (  # noqa: F401
     attention_bwd_head, attention_bwd_dq_rows, attention_bwd_kv_rows, visible_pairs_per_device,
     block_rectangle_work, block_pair_attention,
 )
+from .decode import decode_attention, decode_blocks, ring_decode, decode_batch  # noqa: F401

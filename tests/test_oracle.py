@@ -389,3 +389,87 @@ def test_visible_pairs_brute_force_and_balance():
     assert cont.tolist() == [i * c * c + c * (c + 1) // 2 for i in range(N)]
     assert strp.tolist() == [N * c * (c - 1) // 2 + c * (i + 1) for i in range(N)]
     assert cont.max() / cont.min() > 2 * N - 2 and strp.max() / strp.min() < 1.001
+
+
+# ---------------------------------------------------------------- ring decode
+def _brute_force_decode(q, k, v):
+    """Scalar loops, no max subtraction: o = sum_t w_t v_t / sum_t w_t, w_t = e^{q.k_t/sqrt(D)}."""
+    D = len(q)
+    w = [math.exp(sum(q[x] * kt[x] for x in range(D)) / math.sqrt(D)) for kt in k]
+    tot = sum(w)
+    return np.array([sum(w[t] * v[t][x] for t in range(len(k))) / tot for x in range(D)]), math.log(tot)
+
+
+@pytest.mark.parametrize("L,D", [(1, 3), (5, 4), (17, 8)])
+def test_decode_brute_force(L, D):
+    rng = np.random.default_rng(40 + L)
+    q, k, v = _rand(rng, D), _rand(rng, L, D), _rand(rng, L, D)
+    o, lse = orc.decode_attention(q, k, v)
+    bo, bl = _brute_force_decode(q.tolist(), k.tolist(), v.tolist())
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-12)
+    assert abs(lse - bl) < 1e-12
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_decode_equals_last_row_of_causal_prefill(layout):
+    """The newest token's decode output is the last token's row of full causal
+    attention: its causal mask admits every earlier key."""
+    rng = np.random.default_rng(41)
+    S, D, N = 24, 8, 4
+    q, k, v = _rand(rng, S, D), _rand(rng, S, D), _rand(rng, S, D)
+    pos = orc.token_positions(S, N, layout)
+    last = int(np.argmax(pos))                    # storage row of token S-1
+    ro, rl = orc.attention_rows(q, k, v, [last], N, True, layout)
+    o, lse = orc.decode_attention(q[last], k, v)
+    np.testing.assert_allclose(o, ro[0], rtol=1e-12, atol=1e-12)
+    assert abs(lse - rl[0]) < 1e-12
+
+
+def test_decode_zero_query_is_mean_and_log_count():
+    rng = np.random.default_rng(42)
+    k, v = _rand(rng, 9, 4), _rand(rng, 9, 4)
+    o, lse = orc.decode_attention(np.zeros(4), k, v)
+    np.testing.assert_allclose(o, v.mean(axis=0), rtol=1e-13, atol=1e-13)
+    assert abs(lse - math.log(9)) < 1e-13
+
+
+def test_decode_huge_equal_scores_do_not_overflow():
+    """Scores near 1e4 overflow exp() without the max subtraction; equal keys
+    give the mean of V and lse = s + ln L exactly."""
+    D, L = 4, 6
+    q = np.full(D, 100.0)
+    k = np.full((L, D), 50.0)                     # s = 4 * 5000 / 2 = 10000
+    v = np.arange(L * D, dtype=float).reshape(L, D)
+    o, lse = orc.decode_attention(q, k, v)
+    np.testing.assert_allclose(o, v.mean(axis=0), rtol=1e-13)
+    assert abs(lse - (10000.0 + math.log(L))) < 1e-9
+
+
+def test_decode_blocks_partition_the_cache():
+    for S in (1, 5, 64, 100):
+        for N in (1, 3, 7, 128):
+            blocks = orc.decode_blocks(S, N)
+            assert len(blocks) == N
+            c = -(-S // N)
+            covered = []
+            for j, (a, b) in enumerate(blocks):
+                assert 0 <= a <= b <= S and b - a <= c
+                covered += list(range(a, b))
+            assert covered == list(range(S))
+
+
+@pytest.mark.parametrize("S,N", [(1, 1), (10, 3), (33, 4), (7, 12), (64, 8)])
+def test_ring_decode_blocks_merge_to_the_whole(S, N):
+    """Per-block partials merged in the ring order equal the one-shot
+    definition, also with short and empty trailing blocks (N > S)."""
+    rng = np.random.default_rng(43 + S + N)
+    D = 6
+    q, k, v = _rand(rng, D, scale=2.0), _rand(rng, S, D), _rand(rng, S, D)
+    o, lse = orc.ring_decode(q, k, v, N)
+    ro, rl = orc.decode_attention(q, k, v)
+    np.testing.assert_allclose(o, ro, rtol=1e-12, atol=1e-12)
+    assert abs(lse - rl) < 1e-12
+    for holder in range(N):                       # any host's ring order gives the same state
+        ho, hl = orc.ring_decode(q, k, v, N, holder=holder)
+        np.testing.assert_allclose(ho, ro, rtol=1e-12, atol=1e-12)
+        assert abs(hl - rl) < 1e-12
