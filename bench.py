@@ -1,7 +1,7 @@
 """Benchmark: ring-order blockwise attention forward + backward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k]
+                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k|decode_256k]
 
 A step is one pass of the whole path over one batch of synthetic input: the
 forward (O, LSE) followed by the backward (dQ, dK, dV) from the saved state.
@@ -12,6 +12,9 @@ each) are larger than L2, so no flush is needed between steps.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas; the real multi-GPU ring exchange is not built), the
 timing is the max over ranks and `value` sums the ranks' work.
+
+`--workload decode_256k` measures ring decode instead (one new token against
+a resident 256K-token KV cache; HBM-bound, reported in GB/s).
 
 `--impl reference` times the CPU oracle (float64 NumPy) on the host cores, on
 a bounded sample of the same workload, and prints the same JSON line.
@@ -38,9 +41,9 @@ UNIT = "TFLOP/s"
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was taken on: the hash of csrc/<file> at capture time.
 NCU_TRAFFIC = {
-    "fwd": {"sha256": "f513cc2d013e5a8c62b77b64de25270989a436b4687ea2eed353cf79ea53971c", "workload": "long_128k", "bytes_per_launch": (10.86 + 1.13) * 1e9},
-    "bwd_dkv": {"sha256": "580f1578054763139a07adcf7d41d139b35b5e20e6c8363b06ab83262fe896dc", "workload": "long_128k", "bytes_per_launch": (8.16 + 2.20) * 1e9},
-    "bwd_dq": {"sha256": "580f1578054763139a07adcf7d41d139b35b5e20e6c8363b06ab83262fe896dc", "workload": "long_128k", "bytes_per_launch": (34.87 + 1.08) * 1e9},
+    "fwd": {"sha256": "f378e73e0b1df21a1294517b740fe73238bbc0f982dfa9e7fbb2a2cf4b078779", "workload": "long_128k", "bytes_per_launch": (11.051 + 1.131) * 1e9},
+    "bwd_dkv": {"sha256": "5cbd1598b23ec36503a485eb39e5d3308d3e4079ad2aaa432d85378a4fb5a283", "workload": "long_128k", "bytes_per_launch": (10.250 + 2.279) * 1e9},
+    "bwd_dq": {"sha256": "5cbd1598b23ec36503a485eb39e5d3308d3e4079ad2aaa432d85378a4fb5a283", "workload": "long_128k", "bytes_per_launch": (8.038 + 1.067) * 1e9},
 }
 
 
@@ -411,6 +414,173 @@ def run_balance(args):
     print(json.dumps(out), flush=True)
 
 
+DECODE_METRIC = "ring decode attention KV-cache read GB/s (256K-token context, one new token)"
+
+
+def _decode_bytes(B, H, S, D):
+    """Algorithmic bytes of one decode call: read q, K, V (bf16); write O (bf16), LSE (f32)."""
+    return B * H * (2 * S * D * 2 + D * 2 + D * 2 + 4)
+
+
+def decode_oracle_sample(inp, w, budget_s: float):
+    """Time the oracle's ring decode head by head until `budget_s` is spent.
+    Returns (bytes, seconds, description)."""
+    import oracle as orc
+    B, H, S, D, N = w["B"], w["H"], w["S"], w["D"], w["N"]
+    done, nbytes = 0, 0.0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or done == 0:
+        b, h = divmod(done % (B * H), H)
+        orc.ring_decode(inp["q"][b, h].double().numpy(), inp["k"][b, h].double().numpy(),
+                        inp["v"][b, h].double().numpy(), N)
+        nbytes += _decode_bytes(1, 1, S, D)
+        done += 1
+    dt = time.perf_counter() - t0
+    return nbytes, dt, f"{done} heads of the workload, ring decode of each head in numpy float64"
+
+
+def run_decode(args, w):
+    """Ring decode: one query token per (b, h) against a resident KV cache."""
+    import torch
+    from ring_attention_fwd_gb300.inputs import make_decode_inputs
+    ws, rank, local = _dist()
+    B, H, S, D, N = w["B"], w["H"], w["S"], w["D"], w["N"]
+    cfg = {"workload": args.workload, "B": B, "H": H, "S": S, "D": D, "N": N, "query_tokens": 1,
+           "l2": "KV cache (4.3 GB) larger than L2, no flush",
+           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
+    cores = len(os.sched_getaffinity(0))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = make_decode_inputs(1, 2, S, D, w["seed"], scale=w["scale"])
+        w1 = dict(w, B=1, H=2)
+        per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+        for _ in range(args.warmup):
+            decode_oracle_sample(inp, w1, per_step / 4)
+        tot_b = tot_t = 0.0
+        desc = ""
+        for _ in range(args.steps):
+            nb, t, desc = decode_oracle_sample(inp, w1, per_step)
+            tot_b += nb
+            tot_t += t
+        val = tot_b / tot_t / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC, "value": val, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: {desc}"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import ring_attention_fwd_gb300 as ra
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    inp = make_decode_inputs(B, H, S, D, w["seed"], scale=w["scale"])
+    dev = {k: v.cuda() for k, v in inp.items()}
+    o = torch.empty_like(dev["q"])
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    work = torch.empty(ra.decode_workspace_bytes(B, H, S, D, N), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.decode(dev["q"], dev["k"], dev["v"], N, o=o, lse=lse, workspace=work)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    steps = args.steps * 20          # a call takes well under a millisecond
+    ra.set_kernel_timing(True)
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.3)              # at least one clock sample
+    ktimes = ra.kernel_times()
+    ra.set_kernel_timing(False)
+    ra.check_device_status()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / steps
+    nbytes = _decode_bytes(B, H, S, D)
+    value = nbytes * ws / (ms_step * 1e-3) / 1e9
+    per_kernel = {}
+    for name, ms in ktimes:
+        per_kernel.setdefault(name, []).append(ms)
+    kernels = {n: {"launches": len(l), "ms": statistics.mean(l)} for n, l in per_kernel.items()}
+    split_ms = kernels["decode_split"]["ms"]
+    split_bytes = B * H * (2 * S * D * 2 + D * 2)          # reads q, K, V
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            hbm, hsrc = float(json.load(f)["hbm_gbs"]), "measured copy bandwidth"
+    except Exception:
+        hbm, hsrc = 6800.0, "fallback"
+    achieved = split_bytes / (split_ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get("decode_split")
+    traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash("decode.cu") and \
+        tr["workload"] == args.workload else None
+
+    # end to end: the cache stays resident (it is the server's state); each
+    # step copies the new query in from pinned memory and the result out
+    qh = inp["q"].pin_memory()
+    oh = torch.empty_like(o, device="cpu").pin_memory()
+    lh = torch.empty_like(lse, device="cpu").pin_memory()
+
+    def e2e_step():
+        dev["q"].copy_(qh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / steps
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "tokens_per_s": B * ws / (ms_step * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "decode_split", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "algorithmic_bytes_per_launch": split_bytes,
+                     "avg_launch_ms": split_ms, "peak_kind": hsrc},
+        "e2e": {"value": nbytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": qh.numel() * qh.element_size(),
+                "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size()},
+        "kernels": kernels,
+        "gpu_launches": len(ktimes),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        nb, t, desc = decode_oracle_sample({k: v[:1, :2] for k, v in inp.items()}, dict(w, B=1, H=2),
+                                           args.cpu_seconds)
+        line["cpu_baseline"] = {"value": nb / t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": desc + f"; {t:.1f} s"}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,6 +600,10 @@ def main():
         if args.workload == "long_128k" and "--workload" not in sys.argv:
             args.workload = "balance_32k"
         run_balance(args)
+        return
+    from ring_attention_fwd_gb300.inputs import DECODE_WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        run_decode(args, dict(DECODE_WORKLOADS[args.workload]))
         return
     w = dict(WORKLOADS[args.workload])
     if args.impl == "reference":

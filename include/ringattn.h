@@ -198,6 +198,38 @@ RA_API int ra_bwd_noalloc(const void* Q, const void* K, const void* V, const voi
            int causal, int layout, int dtype, void* stream);
 
 /*
+ * Ring decode ([CH] §5.6: at inference the query has length 1 and the long KV
+ * cache is spread along the ring; [AQ] "超长序列推理与 KV Cache 分发": every
+ * card keeps one segment of the cache; [FT] "局限与未来": split-KV decode).
+ *
+ * ra_decode -- attention of ONE new query token per (b, h) over its whole KV
+ * cache: O = sum_t e^{s_t - LSE} V_t, s_t = q.K_t / sqrt(D), LSE = ln sum_t
+ * e^{s_t}.  The cache's last row is the new token's own key/value, so every
+ * cached key is visible (no mask).  The S cache rows are cut into N ring
+ * blocks, block j = rows [j*c, min((j+1)*c, S)), c = ceil(S/N) (trailing
+ * blocks may be short or empty); each block's partial state is computed from
+ * that block alone and the partials are folded with the LogSumExp merge of
+ * ra_merge.  Called with N = 1 on one block's segment, ra_decode is the
+ * per-host step of a ring: its (O, LSE) chain through ra_merge.
+ *
+ *   q       : [B,H,D] bf16, 16-byte aligned.
+ *   K, V    : [B,H,S,D] bf16 caches, 16-byte aligned.
+ *   O       : [B,H,D] bf16 (output), 2-byte aligned.
+ *   LSE     : [B,H] float32 (output), 4-byte aligned.
+ *   B, H, S, N : >= 1 (N > S allowed: the extra blocks are empty).
+ *   D       : 128.   dtype : RA_BF16.
+ *   workspace, ws_bytes : caller-owned device memory, 256-byte aligned, of at
+ *             least ra_decode_workspace_bytes(B, H, S, D, N) bytes (per-chunk
+ *             partial states; contents on entry are ignored).
+ * Errors: RA_ERR_ARG (null pointer, misalignment, sizes, workspace too small),
+ * RA_ERR_UNSUPPORTED (dtype other than RA_BF16, D != 128), RA_ERR_CUDA.
+ */
+RA_API size_t ra_decode_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N);
+RA_API int ra_decode(const void* q, const void* K, const void* V,
+                     int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, int dtype,
+                     void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * ra_set_timing_buffer -- per-virtual-host time accounting for later bf16
  * ra_fwd calls from any thread (process-wide setting; NULL disables).
  * `dev_buf` is a caller-owned device array of n uint64 that the caller zeroes;
@@ -211,19 +243,20 @@ RA_API int ra_set_timing_buffer(uint64_t* dev_buf, size_t n);
 
 /*
  * Kernel timing (opt-in measurement aid).  ra_set_kernel_timing(1) makes every
- * later ra_fwd / ra_bwd call, from any thread, record CUDA events on its own
+ * later ra_fwd / ra_bwd / ra_decode call, from any thread, record CUDA events on its own
  * stream immediately before and after each kernel it launches; 0 turns it off
  * and drops unread records.  ra_kernel_times() waits for the recorded events,
  * writes one record per timed kernel (oldest call first) and releases them:
  *   call RA_CALL_FWD: kernel 0 = the forward kernel;
  *   call RA_CALL_BWD: kernel 0 = preprocess (D_vec, LSE*log2e),
  *                     kernel 1 = dK/dV kernel, kernel 2 = dQ kernel.
+ *   call RA_CALL_DECODE: kernel 0 = per-chunk partials, kernel 1 = combine.
  * `ms` is the event-to-event time in milliseconds.  *count receives the number
  * of records; if it exceeds `capacity`, the first `capacity` are written, the
  * rest are dropped and RA_ERR_ARG is returned.  The library creates (and keeps
  * for reuse) the events; no device memory is allocated.
  */
-typedef enum { RA_CALL_FWD = 0, RA_CALL_BWD = 1 } ra_call_kind;
+typedef enum { RA_CALL_FWD = 0, RA_CALL_BWD = 1, RA_CALL_DECODE = 2 } ra_call_kind;
 typedef struct {
   int call;     /* ra_call_kind */
   int kernel;   /* index inside the call, see above */

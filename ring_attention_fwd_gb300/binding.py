@@ -35,6 +35,8 @@ SIGNATURES = {
                       _int, _int, _int, _vp, _sz, _vp]),
     "ra_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                               _int, _int, _int, _vp]),
+    "ra_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
+    "ra_decode": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _vp, _fp, _vp, _sz, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
     "ra_set_kernel_timing": (_int, [_int]),
@@ -189,6 +191,41 @@ def bwd_noalloc(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout:
     return dq, dk, dv
 
 
+def decode_workspace_bytes(B, H, S, D, N) -> int:
+    return int(lib().ra_decode_workspace_bytes(B, H, S, D, N))
+
+
+def decode(q, k, v, n_blocks: int = 1, *, o=None, lse=None, workspace=None, stream=None):
+    """Ring decode: one new query token per (b, h) against its KV cache.
+
+    q: [B, H, D]; k, v: [B, H, S, D] (bf16 CUDA tensors).  The cache is cut
+    into ``n_blocks`` ring blocks of ceil(S / n_blocks) rows whose partial
+    states are LogSumExp-merged.  With n_blocks = 1 on one block's segment it
+    is the per-host ring step (chain the results with merge()).
+    Returns (o [B, H, D], lse [B, H] float32)."""
+    _need(q, "q")
+    _need(k, "k", q.dtype)
+    _need(v, "v", q.dtype)
+    if q.dtype not in _DTYPE:
+        raise ValueError("dtype must be bfloat16 or float32")
+    B, H, S, D = k.shape
+    if tuple(q.shape) != (B, H, D) or tuple(v.shape) != (B, H, S, D):
+        raise ValueError("q must be [B, H, D] and v the shape of k")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _need(o, "o", q.dtype)
+    _need(lse, "lse", torch.float32)
+    if workspace is None:
+        need = decode_workspace_bytes(B, H, S, D, int(n_blocks))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib().ra_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, S, D, int(n_blocks), _DTYPE[q.dtype],
+                           o.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return o, lse
+
+
 def set_timing_buffer(buf):
     """Enable per-(virtual host, ring step) timing into a uint64/int64 CUDA
     tensor of >= N*N entries (caller zeroes it); None disables."""
@@ -203,12 +240,13 @@ class KernelTime(ctypes.Structure):
     _fields_ = [("call", ctypes.c_int), ("kernel", ctypes.c_int), ("ms", ctypes.c_float)]
 
 
-KERNEL_NAMES = {(0, 0): "fwd", (1, 0): "bwd_prep", (1, 1): "bwd_dkv", (1, 2): "bwd_dq"}
+KERNEL_NAMES = {(0, 0): "fwd", (1, 0): "bwd_prep", (1, 1): "bwd_dkv", (1, 2): "bwd_dq", (2, 0): "decode_split",
+                (2, 1): "decode_combine"}
 
 
 def set_kernel_timing(enable: bool):
-    """Record CUDA events around every later kernel of fwd/bwd calls (see
-    kernel_times)."""
+    """Record CUDA events around every later kernel of fwd/bwd/decode calls
+    (see kernel_times)."""
     _check(lib().ra_set_kernel_timing(int(bool(enable))))
 
 

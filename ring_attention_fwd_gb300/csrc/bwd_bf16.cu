@@ -68,13 +68,6 @@ __device__ __forceinline__ uint64_t kslice(uint64_t d0, int kk) {
 __device__ __forceinline__ uint64_t mnslice(uint64_t d0, int kk) { return sdesc_add(d0, kk * 16 * 128); }
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) { return kslice(kdesc0(tile), kk); }
 __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) { return mnslice(mndesc0(tile), kk); }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Store 128 f32 TMEM columns of this thread's lane as one bf16 row (scaled).
 __device__ __forceinline__ void store_row_bf16(uint32_t tcol, __nv_bfloat16* out, float sc, bool ok, int ncols) {

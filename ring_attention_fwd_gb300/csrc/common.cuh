@@ -127,6 +127,7 @@ enum : unsigned int {
   ST_OK = 0,
   ST_FWD_WAIT = 0x100,  // | role/barrier id
   ST_BWD_WAIT = 0x200,
+  ST_DEC_WAIT = 0x300,
 };
 
 // ----------------------------------------------------------- launchers
@@ -175,5 +176,48 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v, const void* tmap_do);
+
+// Ring decode work split.  The S-row cache of a head is cut into N ring blocks
+// of c = ceil(S/N) rows; each block into cpb chunks of `chunk` rows (a multiple
+// of 64), so that the whole call has about kDecodeItems work items.  Depends on
+// the sizes only, so the workspace size is known without a device.
+struct DecodePlan {
+  int64_t c, chunk, cpb, items;
+};
+constexpr int64_t kDecodeItems = 16 * 152;   // 16 per SM of a 152-SM GB300
+constexpr int64_t kDecodeMinChunk = 256;
+__host__ __forceinline__ bool decode_plan(int64_t BH, int64_t S, int64_t N, DecodePlan* pl) {
+  if (BH < 1 || S < 1 || N < 1 || N > (int64_t{1} << 30)) return false;
+  if (BH > (int64_t{1} << 40) / N) return false;
+  const int64_t c = (S + N - 1) / N;
+  int64_t want = (kDecodeItems + BH * N - 1) / (BH * N);
+  if (want < 1) want = 1;
+  auto up64 = [](int64_t x) { return (x + 63) / 64 * 64; };
+  int64_t chunk = up64((c + want - 1) / want);
+  const int64_t floor_chunk = up64(c) < kDecodeMinChunk ? up64(c) : kDecodeMinChunk;
+  if (chunk < floor_chunk) chunk = floor_chunk;
+  pl->c = c;
+  pl->chunk = chunk;
+  pl->cpb = (c + chunk - 1) / chunk;
+  pl->items = BH * N * pl->cpb;
+  return true;
+}
+
+struct DecodeArgs {
+  const void* q;     // [B, H, D] bf16
+  const void* K;     // [B, H, S, D] bf16
+  const void* V;
+  void* O;           // [B, H, D] bf16
+  float* LSE;        // [B, H]
+  float* part_o;     // [plan.items, D] f32 workspace
+  float* part_lse;   // [plan.items] f32 workspace
+  int64_t B, H, S, N;
+  DecodePlan plan;
+  unsigned int* status;
+  cudaStream_t stream;
+  int num_sms;
+  cudaEvent_t* ev;   // null, or 3 events: before the split kernel, between, after the combine
+};
+cudaError_t launch_decode_bf16(const DecodeArgs& a);
 
 }  // namespace ra

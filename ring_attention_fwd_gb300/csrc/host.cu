@@ -434,3 +434,67 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
 }
 
 }  // extern "C"
+
+namespace {
+// Decode workspace: per-chunk partial outputs [items, D] and LSEs [items].
+struct DecWs {
+  ra::DecodePlan plan;
+  uint64_t o_bytes, total;
+};
+bool dec_ws(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, DecWs* w) {
+  if (B < 1 || H < 1 || S < 1 || D < 1 || N < 1 || D > 4096) return false;
+  if (B > INT_MAX / H) return false;
+  const int64_t bh = B * H;
+  if (bh > INT64_MAX / S || bh * S > INT64_MAX / D / 4) return false;
+  if (!ra::decode_plan(bh, S, N, &w->plan)) return false;
+  if (w->plan.items > INT64_MAX / D / 8) return false;
+  auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
+  w->o_bytes = up(static_cast<uint64_t>(w->plan.items * D) * 4);
+  w->total = w->o_bytes + up(static_cast<uint64_t>(w->plan.items) * 4);
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ra_decode_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_t N) {
+  DecWs w;
+  return dec_ws(B, H, S, D, N, &w) ? static_cast<size_t>(w.total) : 0;
+}
+
+int ra_decode(const void* q, const void* K, const void* V, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+              int dtype, void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream) {
+  if (!q || !K || !V || !O || !LSE || !workspace) return fail(RA_ERR_ARG, "ra_decode: null pointer");
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_ARG, "bad dtype %d", dtype);
+  DecWs w;
+  if (!dec_ws(B, H, S, D, N, &w))
+    return fail(RA_ERR_ARG, "ra_decode: invalid sizes (B=%lld H=%lld S=%lld D=%lld N=%lld)", (long long)B,
+                (long long)H, (long long)S, (long long)D, (long long)N);
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_decode: only the bf16 path is implemented");
+  if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_decode: bf16 path needs D == 128 (got %lld)", (long long)D);
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16))
+    return fail(RA_ERR_ARG, "ra_decode: q, K and V must be 16-byte aligned");
+  if (!aligned(O, 2) || !aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_decode: misaligned O or LSE");
+  if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "ra_decode: workspace must be 256-byte aligned");
+  if (ws_bytes < w.total)
+    return fail(RA_ERR_ARG, "ra_decode: workspace of %zu bytes, %llu needed", ws_bytes,
+                (unsigned long long)w.total);
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  ra::DecodeArgs a;
+  a.q = q; a.K = K; a.V = V; a.O = O; a.LSE = LSE;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.o_bytes);
+  a.B = B; a.H = H; a.S = S; a.N = N;
+  a.plan = w.plan;
+  a.status = d->status;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.num_sms = d->num_sms;
+  a.ev = kt_begin(RA_CALL_DECODE, 2);
+  cudaError_t e = ra::launch_decode_bf16(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ra_decode launch");
+  return RA_OK;
+}
+
+}  // extern "C"

@@ -65,3 +65,33 @@ WORKLOADS = {
     "fwdbwd_64k": dict(B=1, H=32, S=65536, D=128, N=16, causal=True, layout="striped",
                        dtype="bf16", scale=1.0, seed=5, grad=True),
 }
+
+
+def make_decode_inputs(B: int, H: int, S: int, D: int, seed: int, *, scale: float = 1.0) -> dict:
+    """Return {'q' [B, H, D], 'k', 'v' [B, H, S, D]} bf16 CPU tensors for ring
+    decode: one new query token per (b, h) and an S-row KV cache.
+
+    Same recipe as ``make_inputs``: one generator seeded with ``seed``; q first
+    (one ``randn(1, D)`` per (b, h) slab), then K, then V (one ``randn(S, D)``
+    per slab), each times ``scale`` and rounded to bf16 (nearest even)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    for name, rows in (("q", 1), ("k", S), ("v", S)):
+        t = torch.empty((B, H, rows, D), dtype=torch.bfloat16)
+        for b in range(B):
+            for h in range(H):
+                x = torch.randn((rows, D), generator=g, dtype=torch.float32)
+                if scale != 1.0:
+                    x.mul_(scale)
+                t[b, h].copy_(x.to(torch.bfloat16))
+        out[name] = t
+    out["q"] = out["q"][:, :, 0].contiguous()
+    return out
+
+
+# Ring decode workload: one token of a 256K-token context, 32 heads of 128
+# (the 32-host, 256K-context serving example of the reading notes, §5.6).
+DECODE_WORKLOADS = {
+    "decode_256k": dict(B=1, H=32, S=262144, D=128, N=32, scale=1.0, seed=6),
+}

@@ -14,6 +14,11 @@ forwarded).
 The block compute and the merge default to the library's ``fwd_step`` and
 ``merge`` (CUDA tensors, NCCL process group).  Both are parameters, so the
 exchange protocol can be exercised elsewhere with other implementations.
+
+``ring_decode`` is the inference form (reading notes §5.6; "Ring Attention"
+explainer, "超长序列推理与 KV Cache 分发"): every rank keeps one segment of the
+KV cache and decodes the new token's query against it; the small partial
+states, not the cache, then travel the ring.
 """
 from __future__ import annotations
 
@@ -68,4 +73,46 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
                 raise RuntimeError(f"ring round {s}: exchange with ranks {recv_from}/{send_to} timed out")
         if s < n - 1:
             cur_k, cur_v = bufs[s % 2]
+    return o, lse
+
+
+def ring_decode(q, k, v, *, group=None, step=None, merge=None, timeout_s: float | None = None,
+                lse_dtype=torch.float32):
+    """Ring decode for this rank.
+
+    q: the new token's query [B, H, D], the same on every rank; k, v: this
+    rank's cache segment [B, H, c_i, D] (c_i may be 0).  The rank computes its
+    segment's partial state, then for N-1 rounds forwards the partial it last
+    received (first its own) to rank i+1 and merges the one arriving from
+    rank i-1, so every rank ends with the full (o, lse), merged in its ring
+    order i, i-1, ..., i+1.
+    step(q, k, v) -> (o, lse) partial over one segment (default: the library's
+    ``decode`` with one block); merge as for ring_forward.  lse_dtype: the
+    dtype of the LSE that ``step`` returns (used for an empty segment).
+    Returns (o [B, H, D], lse [B, H])."""
+    n = dist.get_world_size(group)
+    i = dist.get_rank(group)
+    if step is None or merge is None:
+        from . import binding
+        step = step or (lambda qq, kk, vv: binding.decode(qq, kk, vv, 1))
+        merge = merge or (lambda o, l, oj, lj: binding.merge(o, l, oj, lj))
+    B, H, D = q.shape
+    if k.shape[2] > 0:
+        own_o, own_l = step(q, k, v)
+    else:   # empty segment: the empty partial
+        own_o = torch.zeros_like(q)
+        own_l = torch.full((B, H), float("-inf"), dtype=lse_dtype, device=q.device)
+    o, lse = own_o.clone(), own_l.clone()
+    send_to, recv_from = (i + 1) % n, (i - 1) % n
+    cur_o, cur_l = own_o, own_l
+    for s in range(1, n):
+        new_o, new_l = torch.empty_like(own_o), torch.empty_like(own_l)
+        ops = [dist.P2POp(dist.isend, cur_o, send_to, group), dist.P2POp(dist.irecv, new_o, recv_from, group),
+               dist.P2POp(dist.isend, cur_l, send_to, group), dist.P2POp(dist.irecv, new_l, recv_from, group)]
+        for r in dist.batch_isend_irecv(ops):
+            ok = r.wait(datetime.timedelta(seconds=timeout_s)) if timeout_s is not None else r.wait()
+            if ok is False:
+                raise RuntimeError(f"decode round {s}: exchange with ranks {recv_from}/{send_to} timed out")
+        merge(o, lse, new_o, new_l)
+        cur_o, cur_l = new_o, new_l
     return o, lse

@@ -26,7 +26,8 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
-        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc", "ra_set_timing_buffer",
+        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc",
+        "ra_decode_workspace_bytes", "ra_decode", "ra_set_timing_buffer",
         "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
@@ -123,6 +124,44 @@ def test_fwd_step_rejects_bad_block_indices(L):
     assert call(4, 0, -1) == 1
     assert call(0, 0, 0) == 1
     assert L.ra_fwd_step(None, FAKE, FAKE, 1, 1, 64, 128, 4, 1, 0, 1, 0, 1, FAKE, FAKE, None) == 1
+
+
+def test_decode_workspace_size(L):
+    """Per-chunk partials: D floats + 1 LSE per work item, each part rounded
+    up to 256 bytes.  The split depends on the sizes only."""
+    up = lambda x: (x + 255) // 256 * 256
+
+    def expect(B, H, S, D, N):
+        bh, c = B * H, -(-S // N)
+        want = max(1, -(-(16 * 152) // (bh * N)))
+        chunk = max(-(-(-(-c // want)) // 64) * 64, min(-(-c // 64) * 64, 256))
+        items = bh * N * -(-c // chunk)
+        return up(items * D * 4) + up(items * 4)
+
+    for args in [(1, 32, 262144, 128, 32), (2, 3, 1000, 128, 3), (1, 1, 1, 128, 1), (1, 2, 5, 128, 9),
+                 (4, 8, 65536, 128, 1)]:
+        assert L.ra_decode_workspace_bytes(*args) == expect(*args), args
+    assert L.ra_decode_workspace_bytes(1, 32, 262144, 128, 32) == up(3072 * 128 * 4) + up(3072 * 4)
+    assert L.ra_decode_workspace_bytes(0, 1, 1, 128, 1) == 0
+    assert L.ra_decode_workspace_bytes(1, 1, 0, 128, 1) == 0
+
+
+def test_decode_rejects_bad_arguments(L):
+    def call(**kw):
+        a = dict(q=FAKE, B=1, H=2, S=300, D=128, N=4, dtype=1, O=FAKE, LSE=FAKE, ws=FAKE, ws_bytes=1 << 30)
+        a.update(kw)
+        return L.ra_decode(a["q"], FAKE, FAKE, a["B"], a["H"], a["S"], a["D"], a["N"], a["dtype"], a["O"],
+                           a["LSE"], a["ws"], a["ws_bytes"], None)
+    assert call(q=None) == 1 and "null" in L.ra_last_error().decode()
+    assert call(S=0) == 1 and "invalid sizes" in L.ra_last_error().decode()
+    assert call(N=0) == 1
+    assert call(dtype=7) == 1
+    assert call(dtype=0) == 2
+    assert call(D=64) == 2
+    assert call(q=FAKE + 8) == 1 and "16-byte" in L.ra_last_error().decode()
+    assert call(LSE=FAKE + 2) == 1
+    assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
+    assert call(ws_bytes=16) == 1 and "workspace" in L.ra_last_error().decode()
 
 
 def test_wait_test_switch_arguments(L):

@@ -100,3 +100,94 @@ def test_ring_forward_reports_a_host_that_left():
         mp.spawn(_worker, args=(2, _free_port(), 24, 8, True, "striped", d, "leave"), nprocs=2, join=True)
         assert os.path.exists(os.path.join(d, "err0.txt"))
         assert not os.path.exists(os.path.join(d, "o0.npy"))
+
+
+# ------------------------------------------------------------------ ring decode
+def _decode_inputs(B, H, S, D, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((B, H, D)), rng.standard_normal((B, H, S, D)), rng.standard_normal((B, H, S, D))
+
+
+def _oracle_partial(q, k, v):
+    """Oracle partial of one cache segment for every (b, h)."""
+    B, H, D = q.shape
+    o, l = np.zeros((B, H, D)), np.zeros((B, H))
+    for b in range(B):
+        for h in range(H):
+            o[b, h], l[b, h] = orc.decode_attention(q[b, h], k[b, h], v[b, h])
+    return o, l
+
+
+def _decode_worker(rank, world, port, B, H, S, D, outdir, mode):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=20))
+    try:
+        from ring_attention_fwd_gb300.ring import ring_decode
+        q, k, v = _decode_inputs(B, H, S, D, 11)
+        blocks = orc.decode_blocks(S, world)
+        partials = [_oracle_partial(q, k[:, :, a:b], v[:, :, a:b]) for (a, b) in blocks]
+        a, b = blocks[rank]
+        merged = []
+
+        def step(qq, kk, vv):
+            assert kk.shape[2] == b - a
+            o, l = _oracle_partial(qq.numpy(), kk.numpy(), vv.numpy())
+            return torch.from_numpy(o), torch.from_numpy(l)
+
+        def merge(o, l, oj, lj):
+            # which block's partial arrived (by value; empty partials compare equal to each other)
+            hits = [j for j, (po, pl) in enumerate(partials)
+                    if np.array_equal(pl, lj.numpy()) and np.array_equal(po, oj.numpy())]
+            merged.append(hits)
+            for bb in range(o.shape[0]):
+                mo, ml = orc.lse_merge(o[bb].numpy(), l[bb].numpy(), oj[bb].numpy(), lj[bb].numpy())
+                o[bb] = torch.from_numpy(mo)
+                l[bb] = torch.from_numpy(ml)
+
+        if mode == "leave" and rank == 1:
+            return
+        try:
+            o, l = ring_decode(torch.from_numpy(q), torch.from_numpy(k[:, :, a:b].copy()),
+                               torch.from_numpy(v[:, :, a:b].copy()), step=step, merge=merge,
+                               timeout_s=3.0 if mode == "leave" else None, lse_dtype=torch.float64)
+        except Exception as e:           # noqa: BLE001 - reported to the parent
+            with open(os.path.join(outdir, f"err{rank}.txt"), "w") as f:
+                f.write(type(e).__name__ + ": " + str(e))
+            return
+        np.save(os.path.join(outdir, f"o{rank}.npy"), o.numpy())
+        np.save(os.path.join(outdir, f"l{rank}.npy"), l.numpy())
+        with open(os.path.join(outdir, f"merged{rank}.txt"), "w") as f:
+            f.write(repr(merged))
+    finally:
+        if mode != "leave":
+            dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,S", [(2, 40), (4, 37), (3, 2)])
+def test_ring_decode_gloo_matches_whole_cache(world, S):
+    """Every rank ends with the decode of the whole cache; rank i merges the
+    partials of blocks i-1, i-2, ... in that order (S=2 on 3 ranks: one empty block)."""
+    B, H, D = 2, 2, 8
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_decode_worker, args=(world, _free_port(), B, H, S, D, d, "ok"), nprocs=world, join=True)
+        q, k, v = _decode_inputs(B, H, S, D, 11)
+        ro, rl = orc.decode_batch(q, k, v, world)
+        blocks = orc.decode_blocks(S, world)
+        for r in range(world):
+            assert not os.path.exists(os.path.join(d, f"err{r}.txt")), open(os.path.join(d, f"err{r}.txt")).read()
+            np.testing.assert_allclose(np.load(os.path.join(d, f"o{r}.npy")), ro, atol=1e-12)
+            np.testing.assert_allclose(np.load(os.path.join(d, f"l{r}.npy")), rl, atol=1e-12)
+            merged = eval(open(os.path.join(d, f"merged{r}.txt")).read())   # noqa: S307 - our own repr
+            order = orc.ring_order(r, world)[1:]
+            assert len(merged) == world - 1
+            for hits, j in zip(merged, order):
+                assert j in hits or (blocks[j][0] == blocks[j][1] and hits), (r, merged, order)
+
+
+@pytest.mark.timeout(120)
+def test_ring_decode_reports_a_host_that_left():
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_decode_worker, args=(2, _free_port(), 1, 1, 16, 4, d, "leave"), nprocs=2, join=True)
+        assert os.path.exists(os.path.join(d, "err0.txt"))
+        assert not os.path.exists(os.path.join(d, "o0.npy"))
