@@ -293,6 +293,34 @@ def attention_bwd_head(q, k, v, o, lse, do, n_blocks: int, causal: bool, layout:
     return dQ, dK, dV
 
 
+def block_pair_bwd(q, k, v, o, lse, do, i: int, j: int, n_blocks: int, causal: bool, layout: str):
+    """One ring round of the backward, ONE head: the contributions of query
+    block i against KV block j alone.
+
+    The pages only say the backward, like the forward, sweeps the KV blocks
+    around the ring to accumulate dQ, dK, dV ([CH] §5.2).  Restricting the
+    gradient of ``attention_bwd_head`` to the keys of block j gives, with
+    P_ij = exp(Q_i K_j^T / sqrt(D) - LSE_i) on visible entries (LSE_i the
+    block's FINAL log-sum-exp):
+        dV_j += P_ij^T dO_i,  dS_ij = P_ij * (dO_i V_j^T - rowsum(dO_i * O_i)),
+        dQ_i += dS_ij K_j / sqrt(D),  dK_j += dS_ij^T Q_i / sqrt(D).
+    q, k, v, o, do: float64 [S, D] of the whole head; lse [S].  Returns the
+    three contributions (dq_i, dk_j, dv_j), each [c, D].
+    """
+    S, D = q.shape
+    c = S // n_blocks
+    rq = np.arange(i * c, (i + 1) * c)
+    rk = np.arange(j * c, (j + 1) * c)
+    pos = token_positions(S, n_blocks, layout)
+    s = (q[rq] @ k[rk].T) / np.sqrt(D)
+    ok = visible(pos[rq], pos[rk], causal) & np.isfinite(lse[rq])[:, None]
+    P = np.where(ok, np.exp(np.where(ok, s - lse[rq][:, None], -np.inf)), 0.0)
+    dv = P.T @ do[rq]
+    Dvec = (do[rq] * o[rq]).sum(axis=1)
+    dS = P * (do[rq] @ v[rk].T - Dvec[:, None])
+    return (dS @ k[rk]) / np.sqrt(D), (dS.T @ q[rq]) / np.sqrt(D), dv
+
+
 def attention_bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool, layout: str):
     """Batched ``attention_bwd_head``: all float64 [B, H, S, D] (lse [B, H, S])."""
     B, H = q.shape[:2]

@@ -473,3 +473,32 @@ def test_ring_decode_blocks_merge_to_the_whole(S, N):
         ho, hl = orc.ring_decode(q, k, v, N, holder=holder)
         np.testing.assert_allclose(ho, ro, rtol=1e-12, atol=1e-12)
         assert abs(hl - rl) < 1e-12
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_pair_backward_sums_to_the_full_gradient(layout, causal):
+    """Summing one query block's round contributions over all KV blocks gives
+    its rows of dQ; summing one KV block's over all query blocks gives its rows
+    of dK and dV (the full gradient is pinned by finite differences above)."""
+    rng = np.random.default_rng(51)
+    S, D, N = 24, 5, 4
+    c = S // N
+    q, k, v, do = (_rand(rng, S, D) for _ in range(4))
+    o, lse = orc.naive_attention(q[None, None], k[None, None], v[None, None], N, causal, layout)
+    o, lse = o[0, 0], lse[0, 0]
+    dQ, dK, dV = orc.attention_bwd_head(q, k, v, o, lse, do, N, causal, layout)
+    sq = np.zeros_like(dQ)
+    sk = np.zeros_like(dK)
+    sv = np.zeros_like(dV)
+    for i in range(N):
+        for j in range(N):
+            a, b, cc = orc.block_pair_bwd(q, k, v, o, lse, do, i, j, N, causal, layout)
+            sq[i * c:(i + 1) * c] += a
+            sk[j * c:(j + 1) * c] += b
+            sv[j * c:(j + 1) * c] += cc
+            if causal and layout == "contiguous" and j > i:
+                assert not a.any() and not b.any() and not cc.any()
+    np.testing.assert_allclose(sq, dQ, atol=1e-12)
+    np.testing.assert_allclose(sk, dK, atol=1e-12)
+    np.testing.assert_allclose(sv, dV, atol=1e-12)
