@@ -42,8 +42,8 @@ UNIT = "TFLOP/s"
 # source it was taken on: the hash of csrc/<file> at capture time.
 NCU_TRAFFIC = {
     "fwd": {"sha256": "f378e73e0b1df21a1294517b740fe73238bbc0f982dfa9e7fbb2a2cf4b078779", "workload": "long_128k", "bytes_per_launch": (11.051 + 1.131) * 1e9},
-    "bwd_dkv": {"sha256": "5cbd1598b23ec36503a485eb39e5d3308d3e4079ad2aaa432d85378a4fb5a283", "workload": "long_128k", "bytes_per_launch": (10.250 + 2.279) * 1e9},
-    "bwd_dq": {"sha256": "5cbd1598b23ec36503a485eb39e5d3308d3e4079ad2aaa432d85378a4fb5a283", "workload": "long_128k", "bytes_per_launch": (8.038 + 1.067) * 1e9},
+    "bwd_dkv": {"sha256": "24f1a4d9f826dcf322a8d7cdff074fa72e6a8c76f21bc368e740cf29c37ff687", "workload": "long_128k", "bytes_per_launch": (11.567 + 2.300) * 1e9},
+    "bwd_dq": {"sha256": "24f1a4d9f826dcf322a8d7cdff074fa72e6a8c76f21bc368e740cf29c37ff687", "workload": "long_128k", "bytes_per_launch": (8.886 + 1.068) * 1e9},
     "decode_split": {"sha256": "cc1673471a60b305918fea7128dd71985116d8cde5fac48687e1004268484946", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
 }
 

@@ -168,6 +168,35 @@ RA_API int ra_bwd(const void* Q, const void* K, const void* V, const void* O,
            void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * ra_bwd_step -- one host and one ring round of the backward: the gradient
+ * contributions of query block i against KV block j, ADDED into float32
+ * accumulators.  In a multi-host ring ([CH] §5.2: the backward, like the
+ * forward, sweeps the KV blocks around the ring), host i keeps dQ_i and the
+ * accumulators dK_j, dV_j travel with K_j, V_j; after N rounds each has
+ * collected every query block's share and returns to its owner.
+ *     P = exp(Q_i K_j^T / sqrt(D) - LSE_i) on the pair's visible entries,
+ *     dV_j += P^T dO_i,  dS = P * (dO_i V_j^T - rowsum(dO_i * O_i)),
+ *     dQ_i += dS K_j / sqrt(D),  dK_j += dS^T Q_i / sqrt(D).
+ * LSE_i and O_i are block i's FINAL forward results (not a partial state).
+ * Masking as in ra_fwd_step: diag-type pairs mask by true token position, a
+ * contiguous causal pair j > i adds nothing (no kernel runs).
+ *
+ *   Q_i, O_i, dO_i : [B,H,c,D] bf16;  LSE_i [B,H,c] float32;
+ *   K_j, V_j : [B,H,c,D] bf16;  dQ_i, dK_j, dV_j : [B,H,c,D] float32
+ *   accumulators (read and written).  All 16-byte aligned (LSE 4-byte).
+ *   B, H, c, N >= 1;  0 <= i, j < N;  D == 128;  dtype RA_BF16.
+ *   workspace : at least ra_bwd_workspace_bytes(B,H,c,D,1) bytes, 256-byte
+ *   aligned.
+ * Errors: RA_ERR_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA.
+ */
+RA_API int ra_bwd_step(const void* Q_i, const void* K_j, const void* V_j, const void* O_i,
+           const float* LSE_i, const void* dO_i,
+           float* dQ_i, float* dK_j, float* dV_j,
+           int64_t B, int64_t H, int64_t c, int64_t D, int64_t N, int64_t i, int64_t j,
+           int causal, int layout, int dtype,
+           void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * ra_bwd_noalloc -- ra_bwd for callers that cannot allocate device memory.
  *
  * No passage of the pages corresponds to this entry point: it exists for

@@ -33,6 +33,8 @@ SIGNATURES = {
     "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                       _int, _int, _int, _vp, _sz, _vp]),
+    "ra_bwd_step": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _fp, _fp, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                           _int, _int, _int, _vp, _sz, _vp]),
     "ra_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                               _int, _int, _int, _vp]),
     "ra_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
@@ -168,6 +170,28 @@ def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "
                         int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], workspace.data_ptr(),
                         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return dq, dk, dv
+
+
+def bwd_step(q_i, k_j, v_j, o_i, lse_i, do_i, dq_i, dk_j, dv_j, n_blocks: int, i: int, j: int,
+             causal: bool = True, layout: str = "contiguous", *, workspace=None, stream=None):
+    """One ring round of the backward: add the contributions of query block i
+    against KV block j into the float32 accumulators dq_i, dk_j, dv_j (in
+    place).  q_i, o_i, do_i, k_j, v_j: [B, H, c, D] bf16; lse_i: block i's
+    final [B, H, c] LSE.  Returns (dq_i, dk_j, dv_j)."""
+    for name, t in (("q_i", q_i), ("k_j", k_j), ("v_j", v_j), ("o_i", o_i), ("do_i", do_i)):
+        _need(t, name, q_i.dtype)
+    _need(lse_i, "lse_i", torch.float32)
+    for name, t in (("dq_i", dq_i), ("dk_j", dk_j), ("dv_j", dv_j)):
+        _need(t, name, torch.float32)
+    B, H, c, D = q_i.shape
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(B, H, c, D, 1), dtype=torch.uint8, device=q_i.device)
+    _check(lib().ra_bwd_step(q_i.data_ptr(), k_j.data_ptr(), v_j.data_ptr(), o_i.data_ptr(), lse_i.data_ptr(),
+                             do_i.data_ptr(), dq_i.data_ptr(), dk_j.data_ptr(), dv_j.data_ptr(), B, H, c, D,
+                             int(n_blocks), int(i), int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype],
+                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                             _stream_ptr(stream)))
+    return dq_i, dk_j, dv_j
 
 
 def bwd_noalloc(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,

@@ -87,6 +87,28 @@ __device__ __forceinline__ void store_row_bf16(uint32_t tcol, __nv_bfloat16* out
   }
 }
 
+// Add ncols f32 TMEM columns of this thread's lane, scaled, into an f32 row in
+// global memory that this thread alone owns (ring-step accumulation).
+__device__ __forceinline__ void add_row_f32(uint32_t tcol, float* out, float sc, bool ok, int ncols) {
+  for (int ch = 0; ch < ncols / 32; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(tcol + ch * 32, v);
+    tmem_ld_wait();
+    if (ok) {
+      float4* dst = reinterpret_cast<float4*>(out + ch * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4) {
+        float4 a = dst[v4];
+        a.x = fmaf(__uint_as_float(v[4 * v4]), sc, a.x);
+        a.y = fmaf(__uint_as_float(v[4 * v4 + 1]), sc, a.y);
+        a.z = fmaf(__uint_as_float(v[4 * v4 + 2]), sc, a.z);
+        a.w = fmaf(__uint_as_float(v[4 * v4 + 3]), sc, a.w);
+        dst[v4] = a;
+      }
+    }
+  }
+}
+
 struct Params {
   RingGeom g;        // kt_w = mb_h = 128
   int S;
@@ -95,9 +117,13 @@ struct Params {
   float inv_sqrt_d;
   const float* lse2;   // [BH][N][n_mb][128]
   const float* dvec;   // [BH][N][n_mb][128]
-  __nv_bfloat16* dQ;
+  __nv_bfloat16* dQ;   // bf16 outputs (accumulate == 0)
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
+  float* dQf;          // f32 accumulators, added to (accumulate == 1)
+  float* dKf;
+  float* dVf;
+  int accumulate;
   unsigned int* status;
 };
 
@@ -440,10 +466,16 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       dkv_ph ^= 1;
       tc_fence_after();
       const int64_t krow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(j) * g.c + lk;
-      if (grp == 0)
+      if (p.accumulate) {
+        if (grp == 0)
+          add_row_f32(T_DV + lane_off, p.dVf + krow * HD, 1.f, key_ok, HD);
+        else
+          add_row_f32(T_DK + lane_off, p.dKf + krow * HD, p.inv_sqrt_d, key_ok, HD);
+      } else if (grp == 0) {
         store_row_bf16(T_DV + lane_off, p.dV + krow * HD, 1.f, key_ok, HD);
-      else
+      } else {
         store_row_bf16(T_DK + lane_off, p.dK + krow * HD, p.inv_sqrt_d, key_ok, HD);
+      }
       tc_fence_before();
       mbar_arrive(&bars->dkv_empty);
     }
@@ -756,7 +788,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       if (!(ok = mbar_wait(&bars->dq_full, dq_ph, wc, ST_BWD_WAIT | 0x19))) break;
       dq_ph ^= 1;
       tc_fence_after();
-      store_row_bf16(T_DQ + lane_off + grp * 64, p.dQ + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
+      if (p.accumulate)
+        add_row_f32(T_DQ + lane_off + grp * 64, p.dQf + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
+      else
+        store_row_bf16(T_DQ + lane_off + grp * 64, p.dQ + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
     }
@@ -823,7 +858,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.g.c = static_cast<int>(a.S / a.N);
   p.g.causal = a.causal;
   p.g.striped = a.striped;
-  p.g.strict = 0;
+  p.g.strict = a.strict;
   p.g.kt_w = BT;
   p.g.n_kt = (p.g.c + BT - 1) / BT;
   p.g.mb_h = BT;
@@ -833,9 +868,13 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a.D)));
   p.lse2 = a.lse2;
   p.dvec = a.dvec;
-  p.dQ = static_cast<__nv_bfloat16*>(a.dQ);
-  p.dK = static_cast<__nv_bfloat16*>(a.dK);
-  p.dV = static_cast<__nv_bfloat16*>(a.dV);
+  p.accumulate = a.accumulate;
+  p.dQ = a.accumulate ? nullptr : static_cast<__nv_bfloat16*>(a.dQ);
+  p.dK = a.accumulate ? nullptr : static_cast<__nv_bfloat16*>(a.dK);
+  p.dV = a.accumulate ? nullptr : static_cast<__nv_bfloat16*>(a.dV);
+  p.dQf = a.accumulate ? static_cast<float*>(a.dQ) : nullptr;
+  p.dKf = a.accumulate ? static_cast<float*>(a.dK) : nullptr;
+  p.dVf = a.accumulate ? static_cast<float*>(a.dV) : nullptr;
   p.status = a.status;
   const CUtensorMap& mq = *static_cast<const CUtensorMap*>(tmap_q);
   const CUtensorMap& mk = *static_cast<const CUtensorMap*>(tmap_k);

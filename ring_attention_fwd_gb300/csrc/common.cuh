@@ -162,13 +162,15 @@ struct BwdArgs {
   const void* O;
   const float* LSE;
   const void* dO;
-  void* dQ;
+  void* dQ;        // bf16 outputs, or f32 accumulators when `accumulate`
   void* dK;
   void* dV;
   float* lse2;     // [B,H,N,ceil(c/128),128] float32 workspace: LSE * log2(e)
   float* dvec;     // same layout: rowsum(dO * O)
   int64_t B, H, S, D, N;
   int causal, striped;
+  int strict;      // see RingGeom::strict (0 for whole-sequence calls)
+  int accumulate;  // 1: add the gradients into f32 dQ/dK/dV instead of writing bf16
   unsigned int* status;
   cudaStream_t stream;
   int num_sms;

@@ -388,25 +388,32 @@ size_t ra_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D, int64_
   return ws_layout(B, H, S, D, N, &w) ? static_cast<size_t>(w.total) : 0;
 }
 
-int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
-           void* dK, void* dV, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, int causal, int layout,
-           int dtype, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// Validates and launches one backward over tensors of S rows cut into N
+// blocks.  `strict` and `accumulate` serve ra_bwd_step.
+int bwd_impl(const char* who, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+             const void* dO, void* dQ, void* dK, void* dV, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
+             int causal, int layout, int dtype, void* workspace, size_t ws_bytes, void* stream, int strict,
+             int accumulate) {
   if (!Q || !K || !V || !O || !LSE || !dO || !dQ || !dK || !dV || !workspace)
-    return fail(RA_ERR_ARG, "ra_bwd: null pointer");
+    return fail(RA_ERR_ARG, "%s: null pointer", who);
   int rc = check_sizes(B, H, S, D, N);
   if (rc != RA_OK) return rc;
   if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
-  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: only the bf16 path is implemented");
-  if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: bf16 path needs D == 128 (got %lld)", (long long)D);
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "%s: only the bf16 path is implemented", who);
+  if (D != 128) return fail(RA_ERR_UNSUPPORTED, "%s: bf16 path needs D == 128 (got %lld)", who, (long long)D);
   const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
   for (const void* p : ptrs)
-    if (!aligned(p, 16)) return fail(RA_ERR_ARG, "ra_bwd: tensors must be 16-byte aligned");
-  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_bwd: LSE must be 4-byte aligned");
-  if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "ra_bwd: workspace must be 256-byte aligned");
+    if (!aligned(p, 16)) return fail(RA_ERR_ARG, "%s: tensors must be 16-byte aligned", who);
+  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "%s: LSE must be 4-byte aligned", who);
+  if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "%s: workspace must be 256-byte aligned", who);
   WsLayout wl;
-  if (!ws_layout(B, H, S, D, N, &wl)) return fail(RA_ERR_ARG, "ra_bwd: workspace size overflows");
+  if (!ws_layout(B, H, S, D, N, &wl)) return fail(RA_ERR_ARG, "%s: workspace size overflows", who);
   if (ws_bytes < wl.total)
-    return fail(RA_ERR_ARG, "ra_bwd: workspace of %zu bytes, %llu needed", ws_bytes, (unsigned long long)wl.total);
+    return fail(RA_ERR_ARG, "%s: workspace of %zu bytes, %llu needed", who, ws_bytes,
+                (unsigned long long)wl.total);
   DevState* d = nullptr;
   if ((rc = device_state(&d)) != RA_OK) return rc;
 
@@ -418,6 +425,8 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
   a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
   a.causal = causal;
   a.striped = layout == RA_STRIPED;
+  a.strict = strict;
+  a.accumulate = accumulate;
   a.status = d->status;
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
@@ -426,11 +435,44 @@ int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
   if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mdo, dO, B * H, S, D, 128)) != RA_OK) return rc;
-  a.ev = kt_begin(RA_CALL_BWD, 3);
+  a.ev = accumulate ? nullptr : kt_begin(RA_CALL_BWD, 3);
   cudaError_t e = ra::launch_bwd_bf16(a, &mq, &mk, &mv, &mdo);
-  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "ra_bwd: kernel not built");
-  if (e != cudaSuccess) return cuda_fail(e, "ra_bwd launch");
+  if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "%s: kernel not built", who);
+  if (e != cudaSuccess) return cuda_fail(e, who);
   return RA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int ra_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+           void* dK, void* dV, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N, int causal, int layout,
+           int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return bwd_impl("ra_bwd", Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, S, D, N, causal, layout, dtype, workspace,
+                  ws_bytes, stream, 0, 0);
+}
+
+int ra_bwd_step(const void* Q_i, const void* K_j, const void* V_j, const void* O_i, const float* LSE_i,
+                const void* dO_i, float* dQ_i, float* dK_j, float* dV_j, int64_t B, int64_t H, int64_t c, int64_t D,
+                int64_t N, int64_t i, int64_t j, int causal, int layout, int dtype, void* workspace,
+                size_t ws_bytes, void* stream) {
+  if (N < 1 || i < 0 || i >= N || j < 0 || j >= N)
+    return fail(RA_ERR_ARG, "ra_bwd_step: need 0 <= i, j < N (i=%lld j=%lld N=%lld)", (long long)i, (long long)j,
+                (long long)N);
+  int rc = check_enums(causal, layout, dtype);
+  if (rc != RA_OK) return rc;
+  const bool striped = layout == RA_STRIPED;
+  if (causal && !striped && j > i) {
+    // No query of block i sees a key of block j: nothing to add.
+    if (!Q_i || !K_j || !V_j || !O_i || !LSE_i || !dO_i || !dQ_i || !dK_j || !dV_j || !workspace)
+      return fail(RA_ERR_ARG, "ra_bwd_step: null pointer");
+    return check_sizes(B, H, c, D, 1);
+  }
+  // The pair as a 1-block problem, masked as in ra_fwd_step.
+  const int pair_causal = (causal && (striped || j == i)) ? 1 : 0;
+  const int strict = (causal && striped && j > i) ? 1 : 0;
+  return bwd_impl("ra_bwd_step", Q_i, K_j, V_j, O_i, LSE_i, dO_i, dQ_i, dK_j, dV_j, B, H, c, D, 1, pair_causal,
+                  layout, dtype, workspace, ws_bytes, stream, strict, 1);
 }
 
 }  // extern "C"

@@ -15,6 +15,10 @@ The block compute and the merge default to the library's ``fwd_step`` and
 ``merge`` (CUDA tensors, NCCL process group).  Both are parameters, so the
 exchange protocol can be exercised elsewhere with other implementations.
 
+``ring_backward`` is the training backward: dQ_i stays at host i while the
+float32 accumulators of dK_j, dV_j travel with K_j, V_j; after the N rounds
+one more hop returns each to its owner.
+
 ``ring_decode`` is the inference form (reading notes §5.6; "Ring Attention"
 explainer, "超长序列推理与 KV Cache 分发"): every rank keeps one segment of the
 KV cache and decodes the new token's query against it; the small partial
@@ -116,3 +120,54 @@ def ring_decode(q, k, v, *, group=None, step=None, merge=None, timeout_s: float 
         merge(o, lse, new_o, new_l)
         cur_o, cur_l = new_o, new_l
     return o, lse
+
+
+def _wait_all(reqs, timeout_s, what):
+    for r in reqs:
+        ok = r.wait(datetime.timedelta(seconds=timeout_s)) if timeout_s is not None else r.wait()
+        if ok is False:
+            raise RuntimeError(f"{what}: exchange timed out")
+
+
+def ring_backward(q, k, v, o, lse, do, *, causal: bool = True, layout: str = "contiguous", group=None, step=None,
+                  timeout_s: float | None = None):
+    """Ring backward for this rank's blocks.
+
+    q, k, v, o, do: this rank's blocks [B, H, c, D]; lse: its final [B, H, c]
+    LSE from the forward.  In round s the rank holds KV block j = (i - s) mod N
+    together with the float32 accumulators dK_j, dV_j that travelled with it;
+    it adds query block i's contributions (``step``) to its own dQ_i and to
+    dK_j, dV_j, then passes the four tensors on to rank i+1 (K_j, V_j are sent
+    while the round computes; the accumulators once it is done).  After the
+    last round the accumulators hop once more, which brings each rank's own
+    dK_i, dV_i home.  Contiguous causal rounds j > i add nothing and are
+    skipped (the data is still forwarded).
+    step(q, k_j, v_j, o, lse, do, dq, dk_j, dv_j, n, i, j) adds in place
+    (default: the library's ``bwd_step``).  Returns float32 (dq, dk, dv)."""
+    n = dist.get_world_size(group)
+    i = dist.get_rank(group)
+    if step is None:
+        from . import binding
+
+        def step(qq, kk, vv, oo, ll, dd, gq, gk, gv, nn, ii, jj):
+            binding.bwd_step(qq, kk, vv, oo, ll, dd, gq, gk, gv, nn, ii, jj, causal, layout)
+    send_to, recv_from = (i + 1) % n, (i - 1) % n
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.zeros(q.shape, **f32)
+    cur = [k, v, torch.zeros(k.shape, **f32), torch.zeros(v.shape, **f32)]
+    for s, j in enumerate(ring_order(i, n)):
+        kv_reqs, nxt = [], None
+        if s < n - 1:       # K_j, V_j move on while this round computes
+            nxt = [torch.empty_like(cur[0]), torch.empty_like(cur[1])]
+            kv_reqs = dist.batch_isend_irecv([
+                dist.P2POp(dist.isend, cur[0], send_to, group), dist.P2POp(dist.irecv, nxt[0], recv_from, group),
+                dist.P2POp(dist.isend, cur[1], send_to, group), dist.P2POp(dist.irecv, nxt[1], recv_from, group)])
+        if not (causal and layout == "contiguous" and j > i):
+            step(q, cur[0], cur[1], o, lse, do, dq, cur[2], cur[3], n, i, j)
+        acc = [torch.empty_like(cur[2]), torch.empty_like(cur[3])]
+        acc_reqs = dist.batch_isend_irecv([
+            dist.P2POp(dist.isend, cur[2], send_to, group), dist.P2POp(dist.irecv, acc[0], recv_from, group),
+            dist.P2POp(dist.isend, cur[3], send_to, group), dist.P2POp(dist.irecv, acc[1], recv_from, group)])
+        _wait_all(kv_reqs + acc_reqs, timeout_s, f"backward round {s} with ranks {recv_from}/{send_to}")
+        cur = (nxt or [None, None]) + acc
+    return dq, cur[2], cur[3]

@@ -26,7 +26,7 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
-        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_noalloc",
+        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
         "ra_decode_workspace_bytes", "ra_decode", "ra_set_timing_buffer",
         "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_last_error", "ra_version"])
 
@@ -162,6 +162,24 @@ def test_decode_rejects_bad_arguments(L):
     assert call(LSE=FAKE + 2) == 1
     assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
     assert call(ws_bytes=16) == 1 and "workspace" in L.ra_last_error().decode()
+
+
+def test_bwd_step_rejects_bad_arguments(L):
+    def call(N=4, i=1, j=0, causal=1, layout=0, dtype=1, D=128, ws=FAKE, ws_bytes=1 << 30, c=256):
+        return L.ra_bwd_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, c, D, N, i, j, causal,
+                             layout, dtype, ws, ws_bytes, None)
+    assert call(i=4) == 1 and "0 <= i, j < N" in L.ra_last_error().decode()
+    assert call(j=-1) == 1
+    assert call(N=0) == 1
+    assert call(layout=5) == 1
+    assert call(dtype=0) == 2
+    assert call(D=64) == 2
+    assert call(ws_bytes=16) == 1 and "workspace" in L.ra_last_error().decode()
+    assert call(c=0) == 1
+    # contiguous causal j > i: nothing to add, returns before touching memory
+    assert call(i=0, j=3) == 0
+    assert L.ra_bwd_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 128, 4, 0, 3, 1, 0, 1,
+                         FAKE, 1 << 30, None) == 1
 
 
 def test_wait_test_switch_arguments(L):

@@ -191,3 +191,75 @@ def test_ring_decode_reports_a_host_that_left():
         mp.spawn(_decode_worker, args=(2, _free_port(), 1, 1, 16, 4, d, "leave"), nprocs=2, join=True)
         assert os.path.exists(os.path.join(d, "err0.txt"))
         assert not os.path.exists(os.path.join(d, "o0.npy"))
+
+
+# ------------------------------------------------------------------ ring backward
+def _bwd_worker(rank, world, port, S, D, causal, layout, outdir, mode):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=20))
+    try:
+        from ring_attention_fwd_gb300.ring import ring_backward
+        rng = np.random.default_rng(21)
+        q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+        o, lse = orc.attention_rows(q, k, v, np.arange(S), world, causal, layout)
+        c = S // world
+        blk = lambda x, b: torch.from_numpy(x[b * c:(b + 1) * c].copy())[None, None]
+        seen = []
+
+        def step(qq, kk, vv, oo, ll, dd, gq, gk, gv, n, i, j):
+            assert torch.equal(kk, blk(k, j)) and torch.equal(vv, blk(v, j)), f"rank {i}: wrong block for {j}"
+            assert gq.dtype == torch.float32 and gk.dtype == torch.float32
+            seen.append(j)
+            a, b, cc = orc.block_pair_bwd(q, k, v, o, lse, do, i, j, n, causal, layout)
+            gq[0, 0] += torch.from_numpy(a).float()
+            gk[0, 0] += torch.from_numpy(b).float()
+            gv[0, 0] += torch.from_numpy(cc).float()
+
+        if mode == "leave" and rank == 1:
+            return
+        try:
+            dq, dk, dv = ring_backward(blk(q, rank), blk(k, rank), blk(v, rank), blk(o, rank),
+                                       torch.from_numpy(lse[rank * c:(rank + 1) * c].copy())[None, None],
+                                       blk(do, rank), causal=causal, layout=layout, step=step,
+                                       timeout_s=3.0 if mode == "leave" else None)
+        except Exception as e:           # noqa: BLE001 - reported to the parent
+            with open(os.path.join(outdir, f"err{rank}.txt"), "w") as f:
+                f.write(type(e).__name__ + ": " + str(e))
+            return
+        for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            np.save(os.path.join(outdir, f"{name}{rank}.npy"), t[0, 0].double().numpy())
+        np.save(os.path.join(outdir, f"seen{rank}.npy"), np.array(seen))
+    finally:
+        if mode != "leave":
+            dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,layout,causal", [(2, "contiguous", True), (3, "striped", True),
+                                                 (4, "contiguous", True), (2, "contiguous", False)])
+def test_ring_backward_gloo_matches_full_gradient(world, layout, causal):
+    """Every rank ends with its rows of dQ, dK, dV of the whole sequence; the
+    float32 accumulators limit agreement to ~1e-6 relative."""
+    S, D = 8 * world, 6
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_bwd_worker, args=(world, _free_port(), S, D, causal, layout, d, "ok"), nprocs=world, join=True)
+        rng = np.random.default_rng(21)
+        q, k, v, do = (rng.standard_normal((S, D)) for _ in range(4))
+        o, lse = orc.attention_rows(q, k, v, np.arange(S), world, causal, layout)
+        ref = orc.attention_bwd_head(q, k, v, o, lse, do, world, causal, layout)
+        c = S // world
+        for r in range(world):
+            assert not os.path.exists(os.path.join(d, f"err{r}.txt")), open(os.path.join(d, f"err{r}.txt")).read()
+            for name, full in zip(("dq", "dk", "dv"), ref):
+                np.testing.assert_allclose(np.load(os.path.join(d, f"{name}{r}.npy")), full[r * c:(r + 1) * c],
+                                           atol=1e-5, rtol=1e-5)
+            expect = [j for j in orc.ring_order(r, world) if not (causal and layout == "contiguous" and j > r)]
+            assert np.load(os.path.join(d, f"seen{r}.npy")).tolist() == expect
+
+
+@pytest.mark.timeout(120)
+def test_ring_backward_reports_a_host_that_left():
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_bwd_worker, args=(2, _free_port(), 16, 4, True, "striped", d, "leave"), nprocs=2, join=True)
+        assert os.path.exists(os.path.join(d, "err0.txt"))
+        assert not os.path.exists(os.path.join(d, "dq0.npy"))

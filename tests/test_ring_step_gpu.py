@@ -66,3 +66,69 @@ def test_chained_steps_equal_fused_forward(ra, layout, causal):
         assert max_err(o.double().cpu().numpy(), ro[:, :, sl]) <= TOL["bf16"]["o"]
         assert max_err(lse.cpu().numpy(), rl[:, :, sl]) <= TOL["bf16"]["lse"]
         assert max_err(o.float().cpu().numpy(), o_full[:, :, sl].float().cpu().numpy()) <= TOL["bf16"]["o"]
+
+
+def _grad_tol(ref):
+    return 2e-2 * max(1.0, float(np.abs(ref).max()))
+
+
+def _bwd_inputs(B, H, N, c, seed):
+    inp = make_inputs(B, H, N * c, 128, seed=seed, with_grad=True)
+    q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
+    return inp, q, k, v, do
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_bwd_step_pairs_match_oracle(ra, layout):
+    """One round (query block i, KV block j) added into zeroed float32
+    accumulators equals the oracle's pair contributions (O, LSE: the oracle's
+    final forward state, rounded as the GPU would hold them)."""
+    B, H, N, c = 1, 2, 4, 200
+    inp, q, k, v, do = _bwd_inputs(B, H, N, c, seed=33)
+    ro, rl = orc.naive_attention(q, k, v, N, True, layout)
+    o_dev = torch.from_numpy(ro).to(torch.bfloat16)
+    o64 = o_dev.double().numpy()
+    l_dev = torch.from_numpy(rl).float()
+    l64 = l_dev.double().numpy()
+    blk = lambda t, b: t[:, :, b * c:(b + 1) * c].contiguous().cuda()
+    for i, j in [(2, 2), (2, 0), (0, 3), (3, 1), (1, 2)]:
+        dq, dk, dv = (torch.zeros(B, H, c, 128, device="cuda") for _ in range(3))
+        ra.bwd_step(blk(inp["q"], i), blk(inp["k"], j), blk(inp["v"], j), blk(o_dev, i),
+                    l_dev[:, :, i * c:(i + 1) * c].contiguous().cuda(), blk(inp["do"], i), dq, dk, dv, N, i, j,
+                    True, layout)
+        torch.cuda.synchronize()
+        ra.check_device_status()
+        for h in range(H):
+            rq, rk, rv = orc.block_pair_bwd(q[0, h], k[0, h], v[0, h], o64[0, h], l64[0, h], do[0, h], i, j, N,
+                                            True, layout)
+            for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+                assert max_err(g[0, h].cpu().numpy(), r) <= _grad_tol(r), (i, j, h, name)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_bwd_steps_chained_equal_full_backward(ra, layout):
+    """Every host's N rounds, accumulated in float32 as a ring would (dQ_i at
+    its host, dK_j/dV_j travelling), give the full gradient of the oracle and
+    agree with the fused ra_bwd."""
+    B, H, N, c = 1, 2, 4, 256
+    inp, q, k, v, do = _bwd_inputs(B, H, N, c, seed=34)
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
+    o, lse = ra.fwd(dev["q"], dev["k"], dev["v"], N, True, layout)
+    fq, fk, fv = ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, True, layout)
+    blk = lambda t, b: t[:, :, b * c:(b + 1) * c].contiguous()
+    dq = [torch.zeros(B, H, c, 128, device="cuda") for _ in range(N)]
+    dk = [torch.zeros(B, H, c, 128, device="cuda") for _ in range(N)]
+    dv = [torch.zeros(B, H, c, 128, device="cuda") for _ in range(N)]
+    for i in range(N):
+        for j in orc.ring_order(i, N):
+            ra.bwd_step(blk(dev["q"], i), blk(dev["k"], j), blk(dev["v"], j), blk(o, i), blk(lse, i),
+                        blk(dev["do"], i), dq[i], dk[j], dv[j], N, i, j, True, layout)
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    gq, gk, gv = (torch.cat(x, dim=2).cpu().numpy() for x in (dq, dk, dv))
+    o64 = o.double().cpu().numpy()
+    l64 = lse.double().cpu().numpy()
+    rq, rk, rv = orc.attention_bwd(q, k, v, o64, l64, do, N, True, layout)
+    for name, g, r, f in (("dq", gq, rq, fq), ("dk", gk, rk, fk), ("dv", gv, rv, fv)):
+        assert max_err(g, r) <= _grad_tol(r), name
+        assert max_err(g, f.float().cpu().numpy()) <= _grad_tol(r), name
