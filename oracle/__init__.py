@@ -6,3 +6,4 @@ from .attention import (  # noqa: F401
     block_rectangle_work, block_pair_attention, block_pair_bwd,
 )
 from .decode import decode_attention, decode_blocks, ring_decode, decode_batch  # noqa: F401
+from .ffn import silu, ffn_rows, blockwise_ffn  # noqa: F401

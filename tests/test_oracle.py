@@ -502,3 +502,49 @@ def test_block_pair_backward_sums_to_the_full_gradient(layout, causal):
     np.testing.assert_allclose(sq, dQ, atol=1e-12)
     np.testing.assert_allclose(sk, dK, atol=1e-12)
     np.testing.assert_allclose(sv, dV, atol=1e-12)
+
+
+# ---------------------------------------------------------------- blockwise feedforward
+def _brute_ffn(x, w1, w3, w2):
+    """Scalar loops with math.exp: y_r = sum_j W2[o, j] * silu(a_j) * b_j."""
+    out = []
+    for row in x:
+        hid = []
+        for j in range(len(w1)):
+            a = sum(w1[j][t] * row[t] for t in range(len(row)))
+            b = sum(w3[j][t] * row[t] for t in range(len(row)))
+            hid.append(a / (1.0 + math.exp(-a)) * b)
+        out.append([sum(w2[o][j] * hid[j] for j in range(len(hid))) for o in range(len(w2))])
+    return np.array(out)
+
+
+def test_ffn_brute_force():
+    rng = np.random.default_rng(61)
+    T, h, f = 5, 4, 7
+    x, w1, w3, w2 = _rand(rng, T, h), _rand(rng, f, h), _rand(rng, f, h), _rand(rng, h, f)
+    np.testing.assert_allclose(orc.ffn_rows(x, w1, w3, w2), _brute_ffn(x.tolist(), w1.tolist(), w3.tolist(),
+                                                                     w2.tolist()), rtol=1e-12, atol=1e-12)
+
+
+def test_silu_closed_forms():
+    assert orc.silu(0.0) == 0.0
+    assert abs(orc.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert orc.silu(800.0) == 800.0                    # no overflow: sigmoid -> 1
+    assert orc.silu(-800.0) == 0.0 or abs(orc.silu(-800.0)) < 1e-300
+    a = np.linspace(-6, 6, 25)
+    np.testing.assert_allclose(orc.silu(a) - orc.silu(-a), a, atol=1e-14)   # silu(a) - silu(-a) = a
+
+
+def test_ffn_identity_weights_give_silu_times_x():
+    rng = np.random.default_rng(62)
+    x = _rand(rng, 6, 5)
+    eye = np.eye(5)
+    np.testing.assert_allclose(orc.ffn_rows(x, eye, eye, eye), orc.silu(x) * x, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("T,c", [(10, 3), (8, 8), (9, 20), (7, 1)])
+def test_blockwise_ffn_equals_whole_sequence(T, c):
+    rng = np.random.default_rng(63 + T)
+    h, f = 4, 6
+    x, w1, w3, w2 = _rand(rng, T, h), _rand(rng, f, h), _rand(rng, f, h), _rand(rng, h, f)
+    np.testing.assert_allclose(orc.blockwise_ffn(x, w1, w3, w2, c), orc.ffn_rows(x, w1, w3, w2), atol=1e-13)
