@@ -1,7 +1,7 @@
 """Benchmark: ring-order blockwise attention forward + backward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k|decode_256k]
+                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k|decode_256k|ffn_7b]
 
 A step is one pass of the whole path over one batch of synthetic input: the
 forward (O, LSE) followed by the backward (dQ, dK, dV) from the saved state.
@@ -15,6 +15,9 @@ timing is the max over ranks and `value` sums the ranks' work.
 
 `--workload decode_256k` measures ring decode instead (one new token against
 a resident 256K-token KV cache; HBM-bound, reported in GB/s).
+
+`--workload ffn_7b` measures the blockwise gated feedforward of a LLaMA-7B-shaped
+layer over 16384 tokens in blocks of 4096 (tensor-bound, TFLOP/s).
 
 `--impl reference` times the CPU oracle (float64 NumPy) on the host cores, on
 a bounded sample of the same workload, and prints the same JSON line.
@@ -582,6 +585,151 @@ def run_decode(args, w):
         print(json.dumps(line), flush=True)
 
 
+FFN_METRIC = "blockwise gated FFN TFLOP/s (LLaMA-7B-shaped layer, 16384 tokens, blocks of 4096)"
+
+
+def ffn_oracle_sample(inp, w, budget_s: float):
+    """Time the oracle's feedforward on batches of 16 random rows until
+    `budget_s` is spent.  Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle as orc
+    x = inp["x"]
+    w1, w3, w2 = (inp[k].double().numpy() for k in ("w1", "w3", "w2"))
+    rng = np.random.default_rng(0)
+    rows_done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or rows_done == 0:
+        rows = np.sort(rng.choice(x.shape[0], size=16, replace=False))
+        orc.ffn_rows(x[rows].double().numpy(), w1, w3, w2)
+        rows_done += 16
+    dt = time.perf_counter() - t0
+    return 6.0 * rows_done * w["h"] * w["f"], dt, f"{rows_done} random rows, numpy float64 matmuls"
+
+
+def run_ffn(args, w):
+    """Blockwise gated feedforward of one host's tokens, weights resident."""
+    import torch
+    from ring_attention_fwd_gb300.inputs import make_ffn_inputs
+    ws, rank, local = _dist()
+    T, h, f, c = w["T"], w["h"], w["f"], w["block_rows"]
+    flops = 6.0 * T * h * f
+    cfg = {"workload": args.workload, "tokens": T, "hidden": h, "intermediate": f, "block_rows": c,
+           "ffn": "gated (silu)", "l2": "weights 270 MB + X 134 MB, larger than L2, no flush",
+           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
+    cores = len(os.sched_getaffinity(0))
+    inp = make_ffn_inputs(T, h, f, w["seed"])
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+        ffn_oracle_sample(inp, w, per_step / 4)
+        tot_f = tot_t = 0.0
+        desc = ""
+        for _ in range(args.steps):
+            fl, t, desc = ffn_oracle_sample(inp, w, per_step)
+            tot_f += fl
+            tot_t += t
+        val = tot_f / tot_t / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": FFN_METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    import ring_attention_fwd_gb300 as ra
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = {k: v.cuda() for k, v in inp.items()}
+    y = torch.empty_like(dev["x"])
+    work = torch.empty(ra.ffn_workspace_bytes(T, h, f, c), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.ffn(dev["x"], dev["w1"], dev["w3"], dev["w2"], c, y=y, workspace=work)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ra.set_kernel_timing(True)
+    with ClockSampler(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ktimes = ra.kernel_times()
+    ra.set_kernel_timing(False)
+    ra.check_device_status()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    per_kernel = {}
+    for name, ms in ktimes:
+        per_kernel.setdefault(name, []).append(ms)
+    nblocks = -(-T // c)
+    algo = {"ffn_up": 4.0 * c * h * f, "ffn_down": 2.0 * c * h * f}    # per launch (full blocks)
+    kernels = {}
+    for n, l in per_kernel.items():
+        kernels[n] = {"launches": len(l), "ms": statistics.mean(l)}
+        if n in algo:
+            kernels[n]["tflops"] = algo[n] / (kernels[n]["ms"] * 1e-3) / 1e12
+    burst, sustained, src = _peaks()
+    dom = max(kernels, key=lambda n: kernels[n]["ms"] * kernels[n]["launches"])
+    achieved = kernels[dom]["tflops"]
+    xh = inp["x"].pin_memory()
+    yh = torch.empty_like(y, device="cpu").pin_memory()
+
+    def e2e_step():
+        dev["x"].copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.steps
+    line = {
+        "metric": FFN_METRIC, "value": flops * ws / (ms_step * 1e-3) / 1e12, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
+        "config": cfg, "tokens_per_s": T * ws / (ms_step * 1e-3),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained, "unit": UNIT,
+                     "frac": achieved / sustained, "traffic": None, "algorithmic_flops_per_launch": algo[dom],
+                     "avg_launch_ms": kernels[dom]["ms"], "peak_kind": f"{src} sustained bf16 (burst {burst})",
+                     "frac_of_burst": achieved / burst},
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+                "d2h_bytes_per_step": yh.numel() * yh.element_size()},
+        "kernels": kernels, "blocks_per_step": nblocks,
+        "gpu_launches": len(ktimes),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        fl, t, desc = ffn_oracle_sample(inp, w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": fl / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc + f"; {t:.1f} s"}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,7 +750,10 @@ def main():
             args.workload = "balance_32k"
         run_balance(args)
         return
-    from ring_attention_fwd_gb300.inputs import DECODE_WORKLOADS
+    from ring_attention_fwd_gb300.inputs import DECODE_WORKLOADS, FFN_WORKLOADS
+    if args.workload in FFN_WORKLOADS:
+        run_ffn(args, dict(FFN_WORKLOADS[args.workload]))
+        return
     if args.workload in DECODE_WORKLOADS:
         run_decode(args, dict(DECODE_WORKLOADS[args.workload]))
         return

@@ -259,6 +259,32 @@ RA_API int ra_decode(const void* q, const void* K, const void* V,
                      void* O, float* LSE, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * ra_ffn -- blockwise gated feedforward ([CH] §5.2: the feedforward acts on
+ * each host's own block only and runs blockwise; §5.3: its largest activation
+ * is bounded per block; the experiments use LLaMA-style models, whose
+ * feedforward is the gated one):
+ *     Y = (silu(X W1^T) * (X W3^T)) W2^T,   silu(a) = a / (1 + e^-a).
+ * The T rows of X are processed `block_rows` at a time; the f-wide
+ * intermediate of one block (bf16, in `workspace`) is the only intermediate.
+ * Per block: one tensor-core GEMM with the gate/up pairing fused into its
+ * epilogue, then one for the down projection.
+ *
+ *   X, Y    : [T, h] bf16 (input, output), 16-byte aligned.
+ *   W1, W3  : [f, h] bf16; W2 : [h, f] bf16 (the (out, in) layout of a linear
+ *             layer), 16-byte aligned.
+ *   T, block_rows >= 1;  h a multiple of 256;  f a multiple of 128.
+ *   dtype   : RA_BF16.
+ *   workspace, ws_bytes : at least ra_ffn_workspace_bytes(T, h, f, block_rows)
+ *             bytes (min(block_rows, T) * f bf16), 16-byte aligned.
+ * Errors: RA_ERR_ARG (null pointer, sizes, alignment, workspace too small),
+ * RA_ERR_UNSUPPORTED (dtype), RA_ERR_CUDA.
+ */
+RA_API size_t ra_ffn_workspace_bytes(int64_t T, int64_t h, int64_t f, int64_t block_rows);
+RA_API int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* Y,
+                  int64_t T, int64_t h, int64_t f, int64_t block_rows, int dtype,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * ra_set_timing_buffer -- per-virtual-host time accounting for later bf16
  * ra_fwd calls from any thread (process-wide setting; NULL disables).
  * `dev_buf` is a caller-owned device array of n uint64 that the caller zeroes;
@@ -272,20 +298,22 @@ RA_API int ra_set_timing_buffer(uint64_t* dev_buf, size_t n);
 
 /*
  * Kernel timing (opt-in measurement aid).  ra_set_kernel_timing(1) makes every
- * later ra_fwd / ra_bwd / ra_decode call, from any thread, record CUDA events on its own
+ * later ra_fwd / ra_bwd / ra_decode / ra_ffn call, from any thread, record CUDA events on its own
  * stream immediately before and after each kernel it launches; 0 turns it off
  * and drops unread records.  ra_kernel_times() waits for the recorded events,
  * writes one record per timed kernel (oldest call first) and releases them:
  *   call RA_CALL_FWD: kernel 0 = the forward kernel;
  *   call RA_CALL_BWD: kernel 0 = preprocess (D_vec, LSE*log2e),
  *                     kernel 1 = dK/dV kernel, kernel 2 = dQ kernel.
- *   call RA_CALL_DECODE: kernel 0 = per-chunk partials, kernel 1 = combine.
+ *   call RA_CALL_DECODE: kernel 0 = per-chunk partials, kernel 1 = combine;
+ *   call RA_CALL_FFN: kernel 2b = gated up projection of block b, 2b+1 = its
+ *                     down projection (calls of more than 8 blocks run untimed).
  * `ms` is the event-to-event time in milliseconds.  *count receives the number
  * of records; if it exceeds `capacity`, the first `capacity` are written, the
  * rest are dropped and RA_ERR_ARG is returned.  The library creates (and keeps
  * for reuse) the events; no device memory is allocated.
  */
-typedef enum { RA_CALL_FWD = 0, RA_CALL_BWD = 1, RA_CALL_DECODE = 2 } ra_call_kind;
+typedef enum { RA_CALL_FWD = 0, RA_CALL_BWD = 1, RA_CALL_DECODE = 2, RA_CALL_FFN = 3 } ra_call_kind;
 typedef struct {
   int call;     /* ra_call_kind */
   int kernel;   /* index inside the call, see above */

@@ -39,6 +39,8 @@ SIGNATURES = {
                               _int, _int, _int, _vp]),
     "ra_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_decode": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _vp, _fp, _vp, _sz, _vp]),
+    "ra_ffn_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "ra_ffn": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
     "ra_set_kernel_timing": (_int, [_int]),
@@ -250,6 +252,34 @@ def decode(q, k, v, n_blocks: int = 1, *, o=None, lse=None, workspace=None, stre
     return o, lse
 
 
+def ffn_workspace_bytes(T, h, f, block_rows) -> int:
+    return int(lib().ra_ffn_workspace_bytes(T, h, f, block_rows))
+
+
+def ffn(x, w1, w3, w2, block_rows: int, *, y=None, workspace=None, stream=None):
+    """Blockwise gated feedforward Y = (silu(X W1^T) * (X W3^T)) W2^T.
+
+    x: [T, h]; w1, w3: [f, h]; w2: [h, f] (bf16 CUDA tensors).  Rows are
+    processed ``block_rows`` at a time.  Returns y [T, h]."""
+    for name, t in (("x", x), ("w1", w1), ("w3", w3), ("w2", w2)):
+        _need(t, name, x.dtype)
+    if x.dtype not in _DTYPE:
+        raise ValueError("dtype must be bfloat16 or float32")
+    T, h = x.shape
+    f = w1.shape[0]
+    if tuple(w1.shape) != (f, h) or tuple(w3.shape) != (f, h) or tuple(w2.shape) != (h, f):
+        raise ValueError("w1, w3 must be [f, h] and w2 [h, f]")
+    y = torch.empty_like(x) if y is None else y
+    _need(y, "y", x.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(1, ffn_workspace_bytes(T, h, f, int(block_rows))), dtype=torch.uint8,
+                                device=x.device)
+    _check(lib().ra_ffn(x.data_ptr(), w1.data_ptr(), w3.data_ptr(), w2.data_ptr(), y.data_ptr(), T, h, f,
+                        int(block_rows), _DTYPE[x.dtype], workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return y
+
+
 def set_timing_buffer(buf):
     """Enable per-(virtual host, ring step) timing into a uint64/int64 CUDA
     tensor of >= N*N entries (caller zeroes it); None disables."""
@@ -280,8 +310,13 @@ def kernel_times(capacity: int = 4096):
     buf = (KernelTime * capacity)()
     n = ctypes.c_int(0)
     _check(lib().ra_kernel_times(ctypes.addressof(buf), capacity, ctypes.byref(n)))
-    return [(KERNEL_NAMES.get((buf[k].call, buf[k].kernel), f"{buf[k].call}.{buf[k].kernel}"), buf[k].ms)
-            for k in range(n.value)]
+    return [(_kernel_name(buf[k].call, buf[k].kernel), buf[k].ms) for k in range(n.value)]
+
+
+def _kernel_name(call: int, kernel: int) -> str:
+    if call == 3:                                   # feedforward: up/down per block
+        return "ffn_down" if kernel % 2 else "ffn_up"
+    return KERNEL_NAMES.get((call, kernel), f"{call}.{kernel}")
 
 
 def check_device_status(stream=None):

@@ -128,6 +128,7 @@ enum : unsigned int {
   ST_FWD_WAIT = 0x100,  // | role/barrier id
   ST_BWD_WAIT = 0x200,
   ST_DEC_WAIT = 0x300,
+  ST_FFN_WAIT = 0x400,
 };
 
 // ----------------------------------------------------------- launchers
@@ -221,5 +222,20 @@ struct DecodeArgs {
   cudaEvent_t* ev;   // null, or 3 events: before the split kernel, between, after the combine
 };
 cudaError_t launch_decode_bf16(const DecodeArgs& a);
+
+// One GEMM of the blockwise feedforward: out[M, *] from A [M, K] (tensor map
+// tmap_a) and B [*, K] (maps tmap_b0, tmap_b1), all bf16 K-major.
+//   gated: out[:, N] = silu(A W1^T) * (A W3^T), b0 = W1 [N, K], b1 = W3 [N, K]
+//   plain: out[:, N] = A W^T, b0 = b1 = W [N, K]
+struct FfnGemmArgs {
+  int64_t M, N, K;
+  int gated;
+  void* out;
+  int64_t ldo;
+  unsigned int* status;
+  cudaStream_t stream;
+  int num_sms;
+};
+cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void* tmap_b0, const void* tmap_b1);
 
 }  // namespace ra

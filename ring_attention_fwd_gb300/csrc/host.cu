@@ -80,11 +80,12 @@ std::atomic<size_t> g_timing_n{0};
 // ------------------------------------------------------- kernel timing (opt-in)
 // While enabled, each ra_fwd / ra_bwd call records CUDA events on its stream
 // around its kernels; ra_kernel_times() reads and releases them.
+constexpr int kMaxTimedKernels = 16;
 struct TimedCall {
   int call;           // ra_call_kind
   int nk;             // kernels timed (events = nk + 1)
   int dev;
-  cudaEvent_t ev[4];
+  cudaEvent_t ev[kMaxTimedKernels + 1];
 };
 std::atomic<bool> g_kt_on{false};
 std::mutex g_kt_mu;
@@ -94,7 +95,7 @@ std::map<int, std::vector<cudaEvent_t>> g_kt_pool;   // idle events per device
 // Events for one call of `nk` kernels on the current device, or null when
 // timing is off (or an event cannot be created: the call then runs untimed).
 cudaEvent_t* kt_begin(int call, int nk) {
-  if (!g_kt_on.load()) return nullptr;
+  if (!g_kt_on.load() || nk > kMaxTimedKernels) return nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lk(g_kt_mu);
@@ -536,6 +537,70 @@ int ra_decode(const void* q, const void* K, const void* V, int64_t B, int64_t H,
   a.ev = kt_begin(RA_CALL_DECODE, 2);
   cudaError_t e = ra::launch_decode_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "ra_decode launch");
+  return RA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+int64_t ffn_block_rows(int64_t T, int64_t block_rows) { return block_rows < T ? block_rows : T; }
+bool ffn_sizes_ok(int64_t T, int64_t h, int64_t f, int64_t block_rows) {
+  if (T < 1 || h < 256 || f < 128 || block_rows < 1) return false;
+  if (h % 256 != 0 || f % 128 != 0) return false;
+  if (h > INT_MAX || f > INT_MAX || T > INT_MAX) return false;
+  return T <= INT64_MAX / h / 2 && ffn_block_rows(T, block_rows) <= INT64_MAX / f / 2;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ra_ffn_workspace_bytes(int64_t T, int64_t h, int64_t f, int64_t block_rows) {
+  if (!ffn_sizes_ok(T, h, f, block_rows)) return 0;
+  return static_cast<size_t>((ffn_block_rows(T, block_rows) * f * 2 + 255) / 256 * 256);
+}
+
+int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* Y, int64_t T, int64_t h, int64_t f,
+           int64_t block_rows, int dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!X || !W1 || !W3 || !W2 || !Y || !workspace) return fail(RA_ERR_ARG, "ra_ffn: null pointer");
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_ARG, "bad dtype %d", dtype);
+  if (!ffn_sizes_ok(T, h, f, block_rows))
+    return fail(RA_ERR_ARG, "ra_ffn: need T, block_rows >= 1, h a multiple of 256, f a multiple of 128 "
+                "(T=%lld h=%lld f=%lld block_rows=%lld)", (long long)T, (long long)h, (long long)f,
+                (long long)block_rows);
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_ffn: only the bf16 path is implemented");
+  const void* ptrs[] = {X, W1, W3, W2, Y, workspace};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16)) return fail(RA_ERR_ARG, "ra_ffn: tensors and workspace must be 16-byte aligned");
+  const int64_t c = ffn_block_rows(T, block_rows);
+  if (ws_bytes < static_cast<size_t>(c * f * 2))
+    return fail(RA_ERR_ARG, "ra_ffn: workspace of %zu bytes, %lld needed", ws_bytes, (long long)(c * f * 2));
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  CUtensorMap m1, m3, m2, mh;
+  if ((rc = make_map_bf16(&m1, W1, 1, f, h, 128)) != RA_OK) return rc;
+  if ((rc = make_map_bf16(&m3, W3, 1, f, h, 128)) != RA_OK) return rc;
+  if ((rc = make_map_bf16(&m2, W2, 1, h, f, 128)) != RA_OK) return rc;
+  const int64_t nblocks = (T + c - 1) / c;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t* ev = kt_begin(RA_CALL_FFN, static_cast<int>(2 * nblocks));
+  for (int64_t b = 0; b < nblocks; ++b) {
+    const int64_t r0 = b * c, rows = (T - r0 < c) ? T - r0 : c;
+    const char* xb = static_cast<const char*>(X) + r0 * h * 2;
+    char* yb = static_cast<char*>(Y) + r0 * h * 2;
+    CUtensorMap mx;
+    if ((rc = make_map_bf16(&mx, xb, 1, rows, h, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mh, workspace, 1, rows, f, 128)) != RA_OK) return rc;
+    ra::FfnGemmArgs up{rows, f, h, 1, workspace, f, d->status, st, d->num_sms};
+    ra::FfnGemmArgs down{rows, h, f, 0, yb, h, d->status, st, d->num_sms};
+    if (ev) cudaEventRecord(ev[2 * b], st);
+    cudaError_t e = ra::launch_ffn_gemm(up, &mx, &m1, &m3);
+    if (e != cudaSuccess) return cuda_fail(e, "ra_ffn launch (up)");
+    if (ev) cudaEventRecord(ev[2 * b + 1], st);
+    e = ra::launch_ffn_gemm(down, &mh, &m2, &m2);
+    if (e != cudaSuccess) return cuda_fail(e, "ra_ffn launch (down)");
+  }
+  if (ev) cudaEventRecord(ev[2 * nblocks], st);
   return RA_OK;
 }
 

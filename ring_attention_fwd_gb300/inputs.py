@@ -95,3 +95,30 @@ def make_decode_inputs(B: int, H: int, S: int, D: int, seed: int, *, scale: floa
 DECODE_WORKLOADS = {
     "decode_256k": dict(B=1, H=32, S=262144, D=128, N=32, scale=1.0, seed=6),
 }
+
+
+def make_ffn_inputs(T: int, h: int, f: int, seed: int) -> dict:
+    """Return {'x' [T, h], 'w1', 'w3' [f, h], 'w2' [h, f]} bf16 CPU tensors for
+    the blockwise feedforward (random-init weights of that architecture).
+
+    One generator seeded with ``seed``; drawn in the order x, w1, w3, w2, each
+    one ``randn`` of its full shape; x as drawn, each weight times
+    1/sqrt(fan_in) (fan_in = its second dimension) so activations stay O(1);
+    then rounded to bf16 (nearest even)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    for name, shape in (("x", (T, h)), ("w1", (f, h)), ("w3", (f, h)), ("w2", (h, f))):
+        t = torch.randn(shape, generator=g, dtype=torch.float32)
+        if name != "x":
+            t.mul_(1.0 / float(shape[1]) ** 0.5)
+        out[name] = t.to(torch.bfloat16)
+    return out
+
+
+# Blockwise feedforward workload: the gated feedforward of a LLaMA-7B-shaped
+# layer (hidden 4096, intermediate 11008) over one host's 16384 tokens, in
+# blocks of 4096 rows (the ring block size of the 131072-token workload).
+FFN_WORKLOADS = {
+    "ffn_7b": dict(T=16384, h=4096, f=11008, block_rows=4096, seed=7),
+}

@@ -27,7 +27,7 @@ def declared_symbols():
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
-        "ra_decode_workspace_bytes", "ra_decode", "ra_set_timing_buffer",
+        "ra_decode_workspace_bytes", "ra_decode", "ra_ffn_workspace_bytes", "ra_ffn", "ra_set_timing_buffer",
         "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_last_error", "ra_version"])
 
 
@@ -180,6 +180,25 @@ def test_bwd_step_rejects_bad_arguments(L):
     assert call(i=0, j=3) == 0
     assert L.ra_bwd_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 128, 4, 0, 3, 1, 0, 1,
                          FAKE, 1 << 30, None) == 1
+
+
+def test_ffn_workspace_and_bad_arguments(L):
+    assert L.ra_ffn_workspace_bytes(16384, 4096, 11008, 4096) == 4096 * 11008 * 2
+    assert L.ra_ffn_workspace_bytes(100, 256, 128, 4096) == (100 * 128 * 2 + 255) // 256 * 256
+    assert L.ra_ffn_workspace_bytes(100, 255, 128, 64) == 0
+    assert L.ra_ffn_workspace_bytes(100, 256, 100, 64) == 0
+
+    def call(T=300, h=256, f=384, c=128, dtype=1, ws=FAKE, ws_bytes=1 << 30, X=FAKE):
+        return L.ra_ffn(X, FAKE, FAKE, FAKE, FAKE, T, h, f, c, dtype, ws, ws_bytes, None)
+    assert call(X=None) == 1 and "null" in L.ra_last_error().decode()
+    assert call(h=384) == 1 and "multiple of 256" in L.ra_last_error().decode()
+    assert call(f=200) == 1
+    assert call(T=0) == 1
+    assert call(c=0) == 1
+    assert call(dtype=0) == 2
+    assert call(dtype=5) == 1
+    assert call(X=FAKE + 8) == 1 and "16-byte" in L.ra_last_error().decode()
+    assert call(ws_bytes=1000) == 1 and "workspace" in L.ra_last_error().decode()
 
 
 def test_wait_test_switch_arguments(L):
