@@ -275,7 +275,10 @@ RA_API int ra_decode(const void* q, const void* K, const void* V,
  *   T, block_rows >= 1;  h a multiple of 256;  f a multiple of 128.
  *   dtype   : RA_BF16.
  *   workspace, ws_bytes : at least ra_ffn_workspace_bytes(T, h, f, block_rows)
- *             bytes (min(block_rows, T) * f bf16), 16-byte aligned.
+ *             bytes (the block's intermediate, min(block_rows, T) * f bf16,
+ *             then one 4-byte tile counter per launch), 256-byte aligned; its
+ *             contents on entry do not matter.  Calls sharing a workspace
+ *             must not overlap on the GPU.
  * Errors: RA_ERR_ARG (null pointer, sizes, alignment, workspace too small),
  * RA_ERR_UNSUPPORTED (dtype), RA_ERR_CUDA.
  */

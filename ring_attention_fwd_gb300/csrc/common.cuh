@@ -235,6 +235,8 @@ struct FfnGemmArgs {
   unsigned int* status;
   cudaStream_t stream;
   int num_sms;
+  int overlap_previous;   // 1: may start while the previous launch (of the same call) drains
+  int* tile_counter;      // device int, zero before the launch (dynamic tile scheduler)
 };
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void* tmap_b0, const void* tmap_b1);
 

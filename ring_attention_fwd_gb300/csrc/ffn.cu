@@ -13,13 +13,22 @@
 //   down: Y = H W2^T                    -- B tile = 256 rows of W2.
 // H (block_rows x f, bf16) is the only intermediate: the caller's workspace.
 //
+// Consecutive launches of one call overlap (programmatic dependent launch):
+// every launch after the first may start on SMs the previous one has left,
+// e.g. during the down GEMM's last partial wave.  The up GEMM computes at once
+// and waits for the previous grid only before its first store into H (which
+// the previous down GEMM reads); the down GEMM waits before it loads H.
+//
 // Kernel: persistent, one CTA per SM, 192 threads.  Warp 0 (one thread) loads
 // A and B K-chunks of 64 columns with TMA into a 4-stage ring (48 KB a stage,
 // 128-byte swizzle); warp 1 (one thread) issues tcgen05.mma M=128 N=256 K=16
 // into one of two TMEM accumulators (256 columns each) and commits; warps 2-5
 // drain the other accumulator (one thread per row) while the next tile's
-// MMAs run.  Tiles run M-fastest, so the CTAs working at the same time share
-// the B (weight) tiles in L2 and A stays resident.
+// MMAs run.  Tiles are handed out dynamically (an atomic counter per launch,
+// taken by the TMA thread and passed to the MMA and epilogue warps through a
+// small shared-memory ring), numbered M-fastest so the CTAs working at the
+// same time share the B (weight) tiles in L2 and A stays resident; a CTA that
+// starts early (while the previous launch drains) simply takes more tiles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,9 +51,12 @@ constexpr int THREADS = 192;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;          // 2 s
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0, 0);
+constexpr int TSLOTS = 4;                                  // tile ids in flight per CTA
 
 struct Bars {
   uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain;
+  uint64_t tid_full[TSLOTS], tid_empty[TSLOTS];
+  int tile_id[TSLOTS];
   uint32_t tmem_base;
   int abort;
 };
@@ -57,10 +69,17 @@ struct Params {
   int gated;
   __nv_bfloat16* out;    // row-major, leading dimension ldo
   int64_t ldo;
+  int* tile_counter;     // zero before the launch
   unsigned int* status;
 };
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc(saddr, 16, 1024, SWZ_128B); }
+
+// Programmatic dependent launch: let the next grid of the stream be scheduled,
+// and wait until the previous grid has completed and its writes are visible
+// (both no-ops when the launch did not opt in).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float silu_times(float a, float b) {
   return a * __frcp_rn(1.f + hw_exp2(-a * LOG2E)) * b;
@@ -87,6 +106,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       mbar_init(&bars->acc_empty[b], 128);
     }
     mbar_init(&bars->drain, 1);
+    for (int s = 0; s < TSLOTS; ++s) {
+      mbar_init(&bars->tid_full[s], 1);
+      mbar_init(&bars->tid_empty[s], 1 + 128);   // the MMA thread and the 128 epilogue threads
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -97,6 +120,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int tiles = p.m_tiles * p.n_tiles;
@@ -107,9 +131,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB0);
       tma_prefetch_desc(&tmB1);
+      if (!p.gated) pdl_wait_previous();       // A (= H) is the previous grid's output
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (uint32_t lt = 0; ok; ++lt) {
+        int t = atomicAdd(p.tile_counter, 1);
+        if (t >= tiles) t = -1;                  // no tile left: tell the other roles to stop
+        const int slot = lt % TSLOTS;
+        if (!(ok = mbar_wait(&bars->tid_empty[slot], ((lt / TSLOTS) & 1) ^ 1, wc, ST_FFN_WAIT | 5))) break;
+        bars->tile_id[slot] = t;
+        mbar_arrive(&bars->tid_full[slot]);
+        if (t < 0) break;
         const int m = t % p.m_tiles, n = t / p.m_tiles;
         for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
           const int st = it % STAGES;
@@ -127,9 +159,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      uint32_t it = 0, lt = 0;
+      uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++lt) {
+      for (uint32_t lt = 0; ok; ++lt) {
+        const int slot = lt % TSLOTS;
+        if (!(ok = mbar_wait(&bars->tid_full[slot], (lt / TSLOTS) & 1, wc, ST_FFN_WAIT | 6))) break;
+        const int t = bars->tile_id[slot];
+        mbar_arrive(&bars->tid_empty[slot]);
+        if (t < 0) break;
         const uint32_t buf = lt & 1;
         if (!(ok = mbar_wait(&bars->acc_empty[buf], ((lt >> 1) & 1) ^ 1, wc, ST_FFN_WAIT | 2))) break;
         tc_fence_after();
@@ -155,8 +192,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     // ----------------------------------------------------------- epilogue
     const int quad = warp & 3;                       // TMEM lane quadrant of this warp
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t lt = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+    if (p.gated) pdl_wait_previous();          // the previous grid may still read the out buffer (H)
+    for (uint32_t lt = 0;; ++lt) {
+      const int slot = lt % TSLOTS;
+      if (!mbar_wait(&bars->tid_full[slot], (lt / TSLOTS) & 1, wc, ST_FFN_WAIT | 7)) break;
+      const int t = bars->tile_id[slot];
+      mbar_arrive(&bars->tid_empty[slot]);
+      if (t < 0) break;
       const int m = t % p.m_tiles, n = t / p.m_tiles;
       const uint32_t buf = lt & 1;
       if (!mbar_wait(&bars->acc_full[buf], (lt >> 1) & 1, wc, ST_FFN_WAIT | 4)) break;
@@ -229,13 +271,22 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void
   p.gated = a.gated;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.ldo = a.ldo;
+  p.tile_counter = a.tile_counter;
   p.status = a.status;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);
-  ffn::gemm_kernel<<<grid, ffn::THREADS, ffn::SMEM_BYTES, a.stream>>>(
-      *static_cast<const CUtensorMap*>(tmap_a), *static_cast<const CUtensorMap*>(tmap_b0),
-      *static_cast<const CUtensorMap*>(tmap_b1), p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(ffn::THREADS);
+  cfg.dynamicSmemBytes = ffn::SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, ffn::gemm_kernel, *static_cast<const CUtensorMap*>(tmap_a),
+                            *static_cast<const CUtensorMap*>(tmap_b0), *static_cast<const CUtensorMap*>(tmap_b1), p);
 }
 
 }  // namespace ra

@@ -554,9 +554,12 @@ bool ffn_sizes_ok(int64_t T, int64_t h, int64_t f, int64_t block_rows) {
 
 extern "C" {
 
+// Workspace: the block's intermediate H (block_rows x f bf16), then one tile
+// counter (int) per launch of the call (two per block).
 size_t ra_ffn_workspace_bytes(int64_t T, int64_t h, int64_t f, int64_t block_rows) {
   if (!ffn_sizes_ok(T, h, f, block_rows)) return 0;
-  return static_cast<size_t>((ffn_block_rows(T, block_rows) * f * 2 + 255) / 256 * 256);
+  const int64_t c = ffn_block_rows(T, block_rows), nblocks = (T + c - 1) / c;
+  return static_cast<size_t>((c * f * 2 + 255) / 256 * 256 + (2 * nblocks * 4 + 255) / 256 * 256);
 }
 
 int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* Y, int64_t T, int64_t h, int64_t f,
@@ -571,9 +574,11 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
   const void* ptrs[] = {X, W1, W3, W2, Y, workspace};
   for (const void* q : ptrs)
     if (!aligned(q, 16)) return fail(RA_ERR_ARG, "ra_ffn: tensors and workspace must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(RA_ERR_ARG, "ra_ffn: workspace must be 256-byte aligned");
   const int64_t c = ffn_block_rows(T, block_rows);
-  if (ws_bytes < static_cast<size_t>(c * f * 2))
-    return fail(RA_ERR_ARG, "ra_ffn: workspace of %zu bytes, %lld needed", ws_bytes, (long long)(c * f * 2));
+  const size_t need = ra_ffn_workspace_bytes(T, h, f, block_rows);
+  if (ws_bytes < need) return fail(RA_ERR_ARG, "ra_ffn: workspace of %zu bytes, %zu needed", ws_bytes, need);
+  int* counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + (c * f * 2 + 255) / 256 * 256);
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != RA_OK) return rc;
@@ -583,6 +588,8 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
   if ((rc = make_map_bf16(&m2, W2, 1, h, f, 128)) != RA_OK) return rc;
   const int64_t nblocks = (T + c - 1) / c;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t me = cudaMemsetAsync(counters, 0, static_cast<size_t>(2 * nblocks) * sizeof(int), st);
+  if (me != cudaSuccess) return cuda_fail(me, "ra_ffn: clearing the tile counters");
   cudaEvent_t* ev = kt_begin(RA_CALL_FFN, static_cast<int>(2 * nblocks));
   for (int64_t b = 0; b < nblocks; ++b) {
     const int64_t r0 = b * c, rows = (T - r0 < c) ? T - r0 : c;
@@ -591,8 +598,10 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
     CUtensorMap mx;
     if ((rc = make_map_bf16(&mx, xb, 1, rows, h, 128)) != RA_OK) return rc;
     if ((rc = make_map_bf16(&mh, workspace, 1, rows, f, 128)) != RA_OK) return rc;
-    ra::FfnGemmArgs up{rows, f, h, 1, workspace, f, d->status, st, d->num_sms};
-    ra::FfnGemmArgs down{rows, h, f, 0, yb, h, d->status, st, d->num_sms};
+    // The first launch keeps full stream order (X may come from the caller's
+    // previous kernel); later ones overlap the previous launch's last wave.
+    ra::FfnGemmArgs up{rows, f, h, 1, workspace, f, d->status, st, d->num_sms, b > 0 ? 1 : 0, counters + 2 * b};
+    ra::FfnGemmArgs down{rows, h, f, 0, yb, h, d->status, st, d->num_sms, 1, counters + 2 * b + 1};
     if (ev) cudaEventRecord(ev[2 * b], st);
     cudaError_t e = ra::launch_ffn_gemm(up, &mx, &m1, &m3);
     if (e != cudaSuccess) return cuda_fail(e, "ra_ffn launch (up)");

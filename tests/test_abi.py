@@ -183,8 +183,10 @@ def test_bwd_step_rejects_bad_arguments(L):
 
 
 def test_ffn_workspace_and_bad_arguments(L):
-    assert L.ra_ffn_workspace_bytes(16384, 4096, 11008, 4096) == 4096 * 11008 * 2
-    assert L.ra_ffn_workspace_bytes(100, 256, 128, 4096) == (100 * 128 * 2 + 255) // 256 * 256
+    up = lambda x: (x + 255) // 256 * 256
+    assert L.ra_ffn_workspace_bytes(16384, 4096, 11008, 4096) == 4096 * 11008 * 2 + 256   # + 8 tile counters
+    assert L.ra_ffn_workspace_bytes(100, 256, 128, 4096) == up(100 * 128 * 2) + 256
+    assert L.ra_ffn_workspace_bytes(100000, 256, 128, 1000) == up(1000 * 128 * 2) + up(2 * 100 * 4)
     assert L.ra_ffn_workspace_bytes(100, 255, 128, 64) == 0
     assert L.ra_ffn_workspace_bytes(100, 256, 100, 64) == 0
 
@@ -198,6 +200,7 @@ def test_ffn_workspace_and_bad_arguments(L):
     assert call(dtype=0) == 2
     assert call(dtype=5) == 1
     assert call(X=FAKE + 8) == 1 and "16-byte" in L.ra_last_error().decode()
+    assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
     assert call(ws_bytes=1000) == 1 and "workspace" in L.ra_last_error().decode()
 
 
