@@ -58,9 +58,13 @@ def _worker(rank, world, port, S, D, causal, layout, outdir, mode):
 
         if mode == "leave" and rank == 1:
             return                       # this host leaves before its first send
+        if mode == "late" and rank == 1:
+            import time
+            time.sleep(1.5)              # this host's blocks arrive late, but within the time-out
         try:
             o, l = ring_forward(blk(q, rank), blk(k, rank), blk(v, rank), causal=causal, layout=layout,
-                                step=step, merge=merge, timeout_s=3.0 if mode == "leave" else None)
+                                step=step, merge=merge,
+                                timeout_s={"leave": 3.0, "late": 10.0}.get(mode))
         except Exception as e:           # noqa: BLE001 - reported to the parent
             with open(os.path.join(outdir, f"err{rank}.txt"), "w") as f:
                 f.write(type(e).__name__ + ": " + str(e))
@@ -90,6 +94,22 @@ def test_ring_forward_gloo_matches_full_attention(world, layout, causal):
             order = orc.ring_order(r, world)
             expect = [j for j in order if not (causal and layout == "contiguous" and j > r)]
             assert np.load(os.path.join(d, f"seen{r}.npy")).tolist() == expect
+
+
+@pytest.mark.timeout(120)
+def test_ring_forward_tolerates_a_late_host():
+    """A host whose sends start 1.5 s late (inside the 10 s exchange limit)
+    delays the ring but every rank still gets the exact result."""
+    world, S, D = 3, 36, 8
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_worker, args=(world, _free_port(), S, D, True, "striped", d, "late"), nprocs=world, join=True)
+        q, k, v = _inputs(S, D, 5)
+        c = S // world
+        fo, fl = orc.attention_rows(q, k, v, np.arange(S), world, True, "striped")
+        for r in range(world):
+            assert not os.path.exists(os.path.join(d, f"err{r}.txt")), open(os.path.join(d, f"err{r}.txt")).read()
+            np.testing.assert_allclose(np.load(os.path.join(d, f"o{r}.npy")), fo[r * c:(r + 1) * c], atol=1e-12)
+            np.testing.assert_allclose(np.load(os.path.join(d, f"l{r}.npy")), fl[r * c:(r + 1) * c], atol=1e-12)
 
 
 @pytest.mark.timeout(120)
