@@ -390,6 +390,10 @@ def run_ours(args, w):
         "bwd": ({"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
                  "frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / sustained} if with_bwd else None),
         "tokens_per_s": B * S * ws / (ms_step * 1e-3),
+        "flops_per_step": {"convention": f_step,
+                           "exact_visible_pairs": fl.fwd_flops_exact(B, H, S, D, causal) * (3.5 if with_bwd else 1.0),
+                           "value_exact_tflops": fl.fwd_flops_exact(B, H, S, D, causal) * (3.5 if with_bwd else 1.0)
+                           * ws / (ms_step * 1e-3) / 1e12},
         "roofline": roofline,
         "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,

@@ -46,6 +46,8 @@ BWD_CASES = [
     (1, 1, 128, 8, True, "striped"),        # c = 16
     (1, 3, 2048, 4, True, "striped"),
     (1, 2, 2048, 8, False, "striped"),
+    (3, 2, 768, 3, True, "striped"),        # B > 1, causal
+    (1, 2, 8, 8, True, "contiguous"),       # c = 1: one token per block
 ]
 
 

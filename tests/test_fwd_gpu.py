@@ -46,6 +46,8 @@ BF16_CASES = [
     (1, 3, 2048, 4, True, "striped"),
     (1, 2, 4096, 8, False, "striped"),
     (3, 2, 1536, 6, True, "contiguous"),    # c = 256
+    (1, 2, 8, 8, True, "contiguous"),       # c = 1: one token per block
+    (2, 1, 16, 16, True, "striped"),        # c = 1, striped
 ]
 
 
