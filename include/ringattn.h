@@ -338,6 +338,28 @@ RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
 RA_API int ra_set_wait_test(int enable);
 
 /*
+ * ra_probe_mma -- tensor-core issue-rate probe (measurement aid, no
+ * counterpart on the pages).  One CTA per SM issues `iters` tcgen05.mma
+ * kind::f16 instructions (M = 128, N = n, K = 16, bf16 in, f32 accumulate)
+ * back to back (eight K-slices of a 128-deep tile per loop trip) into one
+ * TMEM accumulator, or alternating between two every `switch_every` MMAs
+ * (0 = never; needs n <= 128), A from shared memory (a_from_tmem = 0) or
+ * TMEM (1), B from shared memory, operands pseudo-random; *clk_per_mma
+ * receives the mean SM clocks per instruction.  `variant` (0..63) adds, per
+ * group of eight MMAs: bit 0 a run-time accumulate flag; bit 1 a commit to an
+ * mbarrier; bit 2 a wait on a completed mbarrier plus a tcgen05 fence; bit 3
+ * (with bit 1) a wait for the group issued two groups earlier; bit 4 (with
+ * bit 1) a wait for the previous group; bit 5 issues from a whole warp (one
+ * elected lane) instead of a single thread.  Synchronous on the legacy default
+ * stream; allocates no device memory.
+ * Errors: RA_ERR_ARG (n not a multiple of 16 in 16..256, iters outside
+ * 1..10^7, switch_every < 0 or with n > 128, variant outside 0..63, null
+ * pointer), RA_ERR_CUDA.
+ */
+RA_API int ra_probe_mma(int a_from_tmem, int n, int iters, int switch_every, int variant,
+                        double* clk_per_mma);
+
+/*
  * ra_check_device_status -- synchronise `stream`, then read and clear the
  * library's device-side status word.  Returns RA_ERR_TIMEOUT if any kernel
  * launched since the previous check gave up a bounded wait (the kernel then

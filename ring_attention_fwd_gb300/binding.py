@@ -43,6 +43,7 @@ SIGNATURES = {
     "ra_ffn": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
+    "ra_probe_mma": (_int, [_int, _int, _int, _int, _int, ctypes.POINTER(ctypes.c_double)]),
     "ra_set_kernel_timing": (_int, [_int]),
     "ra_set_wait_test": (_int, [_int]),
     "ra_kernel_times": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_int)]),
@@ -317,6 +318,16 @@ def _kernel_name(call: int, kernel: int) -> str:
     if call == 3:                                   # feedforward: up/down per block
         return "ffn_down" if kernel % 2 else "ffn_up"
     return KERNEL_NAMES.get((call, kernel), f"{call}.{kernel}")
+
+
+def probe_mma(a_from_tmem: bool, n: int, iters: int = 16000, switch_every: int = 0, variant: int = 0) -> float:
+    """Mean SM clocks per tcgen05.mma (M=128, N=n, K=16) issued back to back,
+    alternating two accumulators every ``switch_every`` MMAs if > 0, with the
+    per-group steps selected by ``variant`` (see ra_probe_mma)."""
+    out = ctypes.c_double(0.0)
+    _check(lib().ra_probe_mma(int(bool(a_from_tmem)), int(n), int(iters), int(switch_every), int(variant),
+                              ctypes.byref(out)))
+    return out.value
 
 
 def check_device_status(stream=None):

@@ -129,6 +129,7 @@ enum : unsigned int {
   ST_BWD_WAIT = 0x200,
   ST_DEC_WAIT = 0x300,
   ST_FFN_WAIT = 0x400,
+  ST_PROBE_WAIT = 0x500,
 };
 
 // ----------------------------------------------------------- launchers
@@ -239,5 +240,9 @@ struct FfnGemmArgs {
   int* tile_counter;      // device int, zero before the launch (dynamic tile scheduler)
 };
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void* tmap_b0, const void* tmap_b1);
+
+// Tensor-core issue-rate probe (synchronous; measurement aid).
+cudaError_t launch_probe_mma(int ts, int n, int iters, int switch_every, int variant, int num_sms,
+                             unsigned int* status, double* clk_per_mma);
 
 }  // namespace ra

@@ -182,7 +182,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one elected
+    // lane issues each tcgen05 instruction.
+    {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, 0, 1);
       uint32_t kv_it = 0, q_ph = 0, pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
@@ -194,15 +196,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + q * 128, sdesc_add(dq0, off), sdesc_add(dk0, off), IDESC_QK, kk > 0);
+          mma_ss_w(tmem + q * 128, sdesc_add(dq0, off), sdesc_add(dk0, off), IDESC_QK, kk > 0);
         }
-        mma_commit(&s_full[q]);
+        mma_commit_w(&s_full[q]);
       };
       auto issue_pv = [=](int q, int st, uint32_t acc) {
         const uint64_t dv0 = vmn_desc(sbase + OFF_V + st * TILE_BYTES, 0);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, sdesc_add(dv0, kk * 16 * 128), IDESC_PV,
+          mma_ts_w(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, sdesc_add(dv0, kk * 16 * 128), IDESC_PV,
                  (kk > 0) | acc);
       };
       for (int64_t r = 0; ok; ++r) {
@@ -210,11 +212,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
         const int T = unit_tiles(g, w.i, w.r0);
-        if (!(ok = mbar_wait(&bars->q_full, q_ph, wc, ST_FWD_WAIT | 3))) break;
+        if (!(ok = mbar_wait_w(&bars->q_full, q_ph, wc, ST_FWD_WAIT | 3))) break;
         q_ph ^= 1;
         {
           const int st = kv_it % NSTAGE;
-          if (!(ok = mbar_wait(&bars->k_full[st], (kv_it / NSTAGE) & 1, wc, ST_FWD_WAIT | 4))) break;
+          if (!(ok = mbar_wait_w(&bars->k_full[st], (kv_it / NSTAGE) & 1, wc, ST_FWD_WAIT | 4))) break;
           tc_fence_after();
           issue_s(0, st);
           issue_s(1, st);
@@ -224,23 +226,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const uint32_t ph = (kv_it / NSTAGE) & 1;
           const int nst = (kv_it + 1) % NSTAGE;
           const uint32_t nph = ((kv_it + 1) / NSTAGE) & 1;
-          if (!(ok = mbar_wait(&bars->v_full[st], ph, wc, ST_FWD_WAIT | 5))) break;
+          if (!(ok = mbar_wait_w(&bars->v_full[st], ph, wc, ST_FWD_WAIT | 5))) break;
           for (int q = 0; q < 2 && ok; ++q) {
             if (t == 0 && !first) {
-              if (!(ok = mbar_wait(&bars->o_empty[q], oe_ph[q], wc, ST_FWD_WAIT | 6))) break;
+              if (!(ok = mbar_wait_w(&bars->o_empty[q], oe_ph[q], wc, ST_FWD_WAIT | 6))) break;
               oe_ph[q] ^= 1;
             }
-            if (!(ok = mbar_wait(&bars->p_full[q], pf_ph[q], wc, ST_FWD_WAIT | 7))) break;
+            if (!(ok = mbar_wait_w(&bars->p_full[q], pf_ph[q], wc, ST_FWD_WAIT | 7))) break;
             pf_ph[q] ^= 1;
             tc_fence_after();
             issue_pv(q, st, t > 0 ? 1u : 0u);
-            if (q == 1) mma_commit(&bars->kv_empty[st]);
+            if (q == 1) mma_commit_w(&bars->kv_empty[st]);
             if (t == T - 1) {
-              if (q == 0) mma_commit(&bars->q_empty);
-              mma_commit(&bars->o_full[q]);
+              if (q == 0) mma_commit_w(&bars->q_empty);
+              mma_commit_w(&bars->o_full[q]);
             } else {
               if (q == 0) {
-                if (!(ok = mbar_wait(&bars->k_full[nst], nph, wc, ST_FWD_WAIT | 8))) break;
+                if (!(ok = mbar_wait_w(&bars->k_full[nst], nph, wc, ST_FWD_WAIT | 8))) break;
                 tc_fence_after();
               }
               issue_s(q, nst);
@@ -250,7 +252,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         first = false;
       }
       // Make sure every MMA has finished before TMEM is released.
-      mma_commit(&bars->drain);
+      mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else {

@@ -614,3 +614,24 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
 }
 
 }  // extern "C"
+
+extern "C" {
+
+int ra_probe_mma(int a_from_tmem, int n, int iters, int switch_every, int variant, double* clk_per_mma) {
+  if (!clk_per_mma) return fail(RA_ERR_ARG, "ra_probe_mma: null pointer");
+  if (a_from_tmem != 0 && a_from_tmem != 1) return fail(RA_ERR_ARG, "ra_probe_mma: a_from_tmem must be 0 or 1");
+  if (n < 16 || n > 256 || n % 16 != 0) return fail(RA_ERR_ARG, "ra_probe_mma: n must be a multiple of 16 in 16..256");
+  if (iters < 1 || iters > 10000000) return fail(RA_ERR_ARG, "ra_probe_mma: iters must be in 1..10^7");
+  if (switch_every < 0 || (switch_every > 0 && n > 128))
+    return fail(RA_ERR_ARG, "ra_probe_mma: switch_every >= 0, and two accumulators need n <= 128");
+  if (variant < 0 || variant > 63) return fail(RA_ERR_ARG, "ra_probe_mma: variant must be in 0..63");
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  cudaError_t e =
+      ra::launch_probe_mma(a_from_tmem, n, iters, switch_every, variant, d->num_sms, d->status, clk_per_mma);
+  if (e != cudaSuccess) return cuda_fail(e, "ra_probe_mma");
+  return RA_OK;
+}
+
+}  // extern "C"

@@ -28,7 +28,8 @@ def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
         "ra_decode_workspace_bytes", "ra_decode", "ra_ffn_workspace_bytes", "ra_ffn", "ra_set_timing_buffer",
-        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_last_error", "ra_version"])
+        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_probe_mma",
+        "ra_last_error", "ra_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -202,6 +203,18 @@ def test_ffn_workspace_and_bad_arguments(L):
     assert call(X=FAKE + 8) == 1 and "16-byte" in L.ra_last_error().decode()
     assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
     assert call(ws_bytes=1000) == 1 and "workspace" in L.ra_last_error().decode()
+
+
+def test_probe_rejects_bad_arguments(L):
+    out = ctypes.c_double(0.0)
+    assert L.ra_probe_mma(0, 100, 10, 0, 0, ctypes.byref(out)) == 1 and "multiple of 16" in L.ra_last_error().decode()
+    assert L.ra_probe_mma(0, 512, 10, 0, 0, ctypes.byref(out)) == 1
+    assert L.ra_probe_mma(2, 128, 10, 0, 0, ctypes.byref(out)) == 1
+    assert L.ra_probe_mma(0, 128, 0, 0, 0, ctypes.byref(out)) == 1
+    assert L.ra_probe_mma(0, 256, 10, 8, 0, ctypes.byref(out)) == 1 and "n <= 128" in L.ra_last_error().decode()
+    assert L.ra_probe_mma(0, 128, 10, -1, 0, ctypes.byref(out)) == 1
+    assert L.ra_probe_mma(0, 128, 10, 0, 64, ctypes.byref(out)) == 1
+    assert L.ra_probe_mma(0, 128, 10, 0, 0, None) == 1
 
 
 def test_wait_test_switch_arguments(L):
