@@ -300,7 +300,9 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one elected
+    // lane issues each tcgen05 instruction.
+    {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A, B K-major, N = 128
       constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A from TMEM, B MN-major
@@ -310,12 +312,12 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       auto issue_s = [=](int st) {   // S^T = K Q^T
         const uint64_t bq = kdesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_S, kslice(dK0, kk), kslice(bq, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_S, kslice(dK0, kk), kslice(bq, kk), ID_KK, kk > 0);
       };
       auto issue_dp = [=](int sd) {  // dP^T = V dO^T
         const uint64_t bdo = kdesc0(sbase + OFF_DO + sd * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kslice(dV0, kk), kslice(bdo, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_DP, kslice(dV0, kk), kslice(bdo, kk), ID_KK, kk > 0);
       };
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
@@ -323,36 +325,36 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         int bh, j, kt;
         unit_at(g, u, bh, j, kt);
         const int T = unit_steps(g, j, kt);
-        if (!(ok = mbar_wait(&bars->kv_full, kv_ph, wc, ST_BWD_WAIT | 3))) break;
+        if (!(ok = mbar_wait_w(&bars->kv_full, kv_ph, wc, ST_BWD_WAIT | 3))) break;
         kv_ph ^= 1;
-        if (!(ok = mbar_wait(&bars->q_full[it % QSTAGE], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 4))) break;
+        if (!(ok = mbar_wait_w(&bars->q_full[it % QSTAGE], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 4))) break;
         if (!first_s) {   // S^T region: the previous tile's S^T must have been read
-          if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
+          if (!(ok = mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
           sf_ph ^= 1;
         }
         first_s = false;
         tc_fence_after();
         issue_s(it % QSTAGE);
-        mma_commit(&bars->s_full);
-        if (!(ok = mbar_wait(&bars->do_full[it % DSTAGE], (it / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
+        mma_commit_w(&bars->s_full);
+        if (!(ok = mbar_wait_w(&bars->do_full[it % DSTAGE], (it / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
         tc_fence_after();
         issue_dp(it % DSTAGE);   // dP^T region: last read by the previous tile's dV / dK MMAs
-        mma_commit(&bars->dp_full);
+        mma_commit_w(&bars->dp_full);
         for (int t = 0; t < T && ok; ++t, ++it) {
           const int st = it % QSTAGE, sd = it % DSTAGE;
           const int nst = (it + 1) % QSTAGE, nsd = (it + 1) % DSTAGE;
           if (t + 1 < T) {   // next tile's S^T as soon as this tile's S^T is in registers
-            if (!(ok = mbar_wait(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
-            if (!(ok = mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
+            if (!(ok = mbar_wait_w(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
+            if (!(ok = mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
             sf_ph ^= 1;
             tc_fence_after();
             issue_s(nst);
-            mma_commit(&bars->s_full);
+            mma_commit_w(&bars->s_full);
           }
-          if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 5))) break;
+          if (!(ok = mbar_wait_w(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 5))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
-            if (!(ok = mbar_wait(&bars->dkv_empty, dkve_ph, wc, ST_BWD_WAIT | 6))) break;
+            if (!(ok = mbar_wait_w(&bars->dkv_empty, dkve_ph, wc, ST_BWD_WAIT | 6))) break;
             dkve_ph ^= 1;
           }
           tc_fence_after();
@@ -360,25 +362,25 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const uint64_t mdo = mndesc0(sbase + OFF_DO + sd * TILE_BYTES), mq = mndesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO
-            mma_ts(T_DV, T_DP + pcol_p(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
-          mma_commit(&bars->do_empty[sd]);
+            mma_ts_w(T_DV, T_DP + pcol_p(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
+          mma_commit_w(&bars->do_empty[sd]);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q
-            mma_ts(T_DK, T_DP + pcol_ds(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
-          mma_commit(&bars->q_empty[st]);
+            mma_ts_w(T_DK, T_DP + pcol_ds(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
+          mma_commit_w(&bars->q_empty[st]);
           if (t + 1 < T) {
-            if (!(ok = mbar_wait(&bars->do_full[nsd], ((it + 1) / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
+            if (!(ok = mbar_wait_w(&bars->do_full[nsd], ((it + 1) / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
             tc_fence_after();
             issue_dp(nsd);
-            mma_commit(&bars->dp_full);
+            mma_commit_w(&bars->dp_full);
           }
         }
         if (!ok) break;
-        mma_commit(&bars->kv_empty);
-        mma_commit(&bars->dkv_full);
+        mma_commit_w(&bars->kv_empty);
+        mma_commit_w(&bars->dkv_full);
         first_unit = false;
       }
-      mma_commit(&bars->drain);
+      mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else if (warp >= 4) {
@@ -608,7 +610,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one elected
+    // lane issues each tcgen05 instruction.
+    {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // B K-major, N = 128
       constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A (TMEM), B MN-major
@@ -618,18 +622,18 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       auto issue_s = [=](int st) {   // S = Q K^T  (Q from TMEM)
         const uint64_t bk = kdesc0(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ts(T_S, T_Q + kk * 8, kslice(bk, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ts_w(T_S, T_Q + kk * 8, kslice(bk, kk), ID_KK, kk > 0);
       };
       auto issue_dp = [=](int st) {  // dP = dO V^T  (dO from shared memory)
         const uint64_t bv = kdesc0(sbase + OFF_V + st * TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ss(T_DP, kslice(dDO0, kk), kslice(bv, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_DP, kslice(dDO0, kk), kslice(bv, kk), ID_KK, kk > 0);
       };
       auto wait_kv = [&](uint32_t k_it) -> bool {
         const int st = k_it % KSTAGE;
         const uint32_t ph = (k_it / KSTAGE) & 1;
-        if (!mbar_wait(&bars->k_full[st], ph, wc, ST_BWD_WAIT | 0x14)) return false;
-        if (!mbar_wait(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15)) return false;
+        if (!mbar_wait_w(&bars->k_full[st], ph, wc, ST_BWD_WAIT | 0x14)) return false;
+        if (!mbar_wait_w(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15)) return false;
         return true;
       };
       // S for KV tile k_it once the previous S is in registers, then dP once the
@@ -637,21 +641,21 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       auto issue_tile = [&](uint32_t k_it) -> bool {
         if (!wait_kv(k_it)) return false;
         if (!first_s) {
-          if (!mbar_wait(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c)) return false;
+          if (!mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c)) return false;
           sf_ph ^= 1;
         }
         first_s = false;
         tc_fence_after();
         issue_s(k_it % KSTAGE);
-        mma_commit(&bars->s_full);
+        mma_commit_w(&bars->s_full);
         if (!first_dp) {
-          if (!mbar_wait(&bars->dp_free, df_ph, wc, ST_BWD_WAIT | 0x1d)) return false;
+          if (!mbar_wait_w(&bars->dp_free, df_ph, wc, ST_BWD_WAIT | 0x1d)) return false;
           df_ph ^= 1;
         }
         first_dp = false;
         tc_fence_after();
         issue_dp(k_it % KSTAGE);
-        mma_commit(&bars->dp_full);
+        mma_commit_w(&bars->dp_full);
         return true;
       };
       for (int64_t r = 0; ok; ++r) {
@@ -659,36 +663,36 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         if (u >= p.num_units) break;
         const Unit w = unit_at(g, u);
         const int T = unit_tiles(g, w.i, w.r0);
-        if (!(ok = mbar_wait(&bars->do_full, de_ph, wc, ST_BWD_WAIT | 0x13))) break;
+        if (!(ok = mbar_wait_w(&bars->do_full, de_ph, wc, ST_BWD_WAIT | 0x13))) break;
         de_ph ^= 1;
-        if (!(ok = mbar_wait(&bars->qo_full, qo_ph, wc, ST_BWD_WAIT | 0x1e))) break;
+        if (!(ok = mbar_wait_w(&bars->qo_full, qo_ph, wc, ST_BWD_WAIT | 0x1e))) break;
         qo_ph ^= 1;
         if (!(ok = issue_tile(it))) break;
         for (int t = 0; t < T && ok; ++t, ++it) {
           const int st = it % KSTAGE;
           if (t + 1 < T && !(ok = issue_tile(it + 1))) break;
-          if (!(ok = mbar_wait(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 0x16))) break;
+          if (!(ok = mbar_wait_w(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 0x16))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
-            if (!(ok = mbar_wait(&bars->dq_empty, dqe_ph, wc, ST_BWD_WAIT | 0x17))) break;
+            if (!(ok = mbar_wait_w(&bars->dq_empty, dqe_ph, wc, ST_BWD_WAIT | 0x17))) break;
             dqe_ph ^= 1;
           }
           tc_fence_after();
           const uint64_t mk = mndesc0(sbase + OFF_K + st * TILE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS from TMEM, K MN-major)
-            mma_ts(T_DQ, T_DS + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
-          mma_commit(&bars->ds_free);
-          mma_commit(&bars->kv_empty[st]);
+            mma_ts_w(T_DQ, T_DS + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
+          mma_commit_w(&bars->ds_free);
+          mma_commit_w(&bars->kv_empty[st]);
           if (t == T - 1) {
-            mma_commit(&bars->do_empty);
-            mma_commit(&bars->qo_empty);
-            mma_commit(&bars->dq_full);
+            mma_commit_w(&bars->do_empty);
+            mma_commit_w(&bars->qo_empty);
+            mma_commit_w(&bars->dq_full);
           }
         }
         first_unit = false;
       }
-      mma_commit(&bars->drain);
+      mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else if (warp >= 4) {
