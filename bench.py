@@ -49,9 +49,9 @@ UNIT = "TFLOP/s"
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # source it was taken on: the hash of csrc/<file> at capture time.
 NCU_TRAFFIC = {
-    "fwd": {"sha256": "f378e73e0b1df21a1294517b740fe73238bbc0f982dfa9e7fbb2a2cf4b078779", "workload": "long_128k", "bytes_per_launch": (11.051 + 1.131) * 1e9},
-    "bwd_dkv": {"sha256": "24f1a4d9f826dcf322a8d7cdff074fa72e6a8c76f21bc368e740cf29c37ff687", "workload": "long_128k", "bytes_per_launch": (11.567 + 2.300) * 1e9},
-    "bwd_dq": {"sha256": "24f1a4d9f826dcf322a8d7cdff074fa72e6a8c76f21bc368e740cf29c37ff687", "workload": "long_128k", "bytes_per_launch": (8.886 + 1.068) * 1e9},
+    "fwd": {"sha256": "4984ee29123d382ec59c34b8b8812d0820b11b7684c12a2957fa787a1feb7464", "workload": "long_128k", "bytes_per_launch": (10.408 + 1.132) * 1e9},
+    "bwd_dkv": {"sha256": "78cc7300f323f8d4c05ef6c0f7c4482dbeded4512a0b6134ae9b7729458c99e5", "workload": "long_128k", "bytes_per_launch": (10.146 + 2.278) * 1e9},
+    "bwd_dq": {"sha256": "78cc7300f323f8d4c05ef6c0f7c4482dbeded4512a0b6134ae9b7729458c99e5", "workload": "long_128k", "bytes_per_launch": (13.032 + 1.066) * 1e9},
     "decode_split": {"sha256": "cc1673471a60b305918fea7128dd71985116d8cde5fac48687e1004268484946", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
 }
 
