@@ -158,34 +158,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
+    // The whole warp runs the issue loop (warp-uniform operands); one elected
+    // lane issues each tcgen05 instruction.
+    {
       uint32_t it = 0;
       bool ok = true;
       for (uint32_t lt = 0; ok; ++lt) {
         const int slot = lt % TSLOTS;
-        if (!(ok = mbar_wait(&bars->tid_full[slot], (lt / TSLOTS) & 1, wc, ST_FFN_WAIT | 6))) break;
+        if (!(ok = mbar_wait_w(&bars->tid_full[slot], (lt / TSLOTS) & 1, wc, ST_FFN_WAIT | 6))) break;
         const int t = bars->tile_id[slot];
-        mbar_arrive(&bars->tid_empty[slot]);
+        if (lane == 0) mbar_arrive(&bars->tid_empty[slot]);   // one of the 129 arrivals
         if (t < 0) break;
         const uint32_t buf = lt & 1;
-        if (!(ok = mbar_wait(&bars->acc_empty[buf], ((lt >> 1) & 1) ^ 1, wc, ST_FFN_WAIT | 2))) break;
+        if (!(ok = mbar_wait_w(&bars->acc_empty[buf], ((lt >> 1) & 1) ^ 1, wc, ST_FFN_WAIT | 2))) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * BN;
         for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
           const int st = it % STAGES;
-          if (!(ok = mbar_wait(&bars->full[st], (it / STAGES) & 1, wc, ST_FFN_WAIT | 3))) break;
+          if (!(ok = mbar_wait_w(&bars->full[st], (it / STAGES) & 1, wc, ST_FFN_WAIT | 3))) break;
           tc_fence_after();
           const uint64_t a0 = kdesc(sbase + st * STAGE_BYTES);
           const uint64_t b0 = kdesc(sbase + st * STAGE_BYTES + A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_ss(d, sdesc_add(a0, kk * 32), sdesc_add(b0, kk * 32), IDESC, (kc | kk) != 0);
-          mma_commit(&bars->empty[st]);
+            mma_ss_w(d, sdesc_add(a0, kk * 32), sdesc_add(b0, kk * 32), IDESC, (kc | kk) != 0);
+          mma_commit_w(&bars->empty[st]);
         }
         if (!ok) break;
-        mma_commit(&bars->acc_full[buf]);
+        mma_commit_w(&bars->acc_full[buf]);
       }
-      mma_commit(&bars->drain);
+      mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
   } else {
