@@ -494,17 +494,21 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
 // ============================================================== dQ
 namespace q {
-constexpr int KSTAGE = 3;
+// K tiles stream through a 4-stage ring and V tiles through a 2-stage one: K
+// is the first operand a tile needs (S) and the last it releases (dQ += dS K),
+// V is released as soon as dP has been computed.
+constexpr int KSTAGE = 4;
+constexpr int VSTAGE = 2;
 constexpr uint32_t OFF_DO = 0;                              // dO tile of the unit
 constexpr uint32_t OFF_K = OFF_DO + TILE_BYTES;             // KSTAGE tiles
-constexpr uint32_t OFF_V = OFF_K + KSTAGE * TILE_BYTES;     // KSTAGE tiles
-constexpr uint32_t OFF_BAR = OFF_V + KSTAGE * TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + KSTAGE * TILE_BYTES;     // VSTAGE tiles
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGE * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Bars {
   uint64_t do_full, do_empty;
-  uint64_t k_full[KSTAGE], v_full[KSTAGE], kv_empty[KSTAGE];
+  uint64_t k_full[KSTAGE], k_empty[KSTAGE], v_full[VSTAGE], v_empty[VSTAGE];
   uint64_t qo_full, qo_empty, s_full, s_free, dp_full, dp_free, p_full, ds_free, dq_full, dq_empty, drain;
   uint32_t tmem_base;
   int abort;
@@ -531,8 +535,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     mbar_init(&bars->do_empty, 1);
     for (int s = 0; s < KSTAGE; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VSTAGE; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->qo_full, 256);
     mbar_init(&bars->qo_empty, 1);
@@ -570,7 +577,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      uint32_t it = 0, nd = 0, de_ph = 0;
+      uint32_t nk = 0, nv = 0, nd = 0, de_ph = 0;
       bool ok = true;
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
@@ -588,24 +595,28 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           const int j = ring_block(w.i, s, g.N);
           if (!block_visited(g, w.i, j)) continue;
           const int last = kt_last(g, w.i, j, w.r0);
-          for (int kt = 0; kt <= last; ++kt, ++it) {
-            const int st = it % KSTAGE;
-            if (!(ok = mbar_wait(&bars->kv_empty[st], ((it / KSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x12))) break;
+          for (int kt = 0; kt <= last; ++kt) {
             const int krow = j * g.c + kt * BT;
-            mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+            const int sk = nk % KSTAGE;
+            if (!(ok = mbar_wait(&bars->k_empty[sk], ((nk / KSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x12))) break;
+            mbar_arrive_expect_tx(&bars->k_full[sk], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_K + st * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[st], h * 64, krow, w.bh);
-            mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+              tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk], h * 64, krow, w.bh);
+            ++nk;
+            const int sv = nv % VSTAGE;
+            if (!(ok = mbar_wait(&bars->v_empty[sv], ((nv / VSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x1a))) break;
+            mbar_arrive_expect_tx(&bars->v_full[sv], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_V + st * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[st], h * 64, krow, w.bh);
+              tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv], h * 64, krow, w.bh);
+            ++nv;
           }
         }
       }
       if (!ok) {
-        for (uint32_t k = (it > KSTAGE ? it - KSTAGE : 0); k < it; ++k) {
+        for (uint32_t k = (nk > KSTAGE ? nk - KSTAGE : 0); k < nk; ++k)
           mbar_drain(&bars->k_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
-          mbar_drain(&bars->v_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
-        }
+        for (uint32_t k = (nv > VSTAGE ? nv - VSTAGE : 0); k < nv; ++k)
+          mbar_drain(&bars->v_full[k % VSTAGE], (k / VSTAGE) & 1, 200000000ull);
         if (nd > 0) mbar_drain(&bars->do_full, (nd - 1) & 1, 200000000ull);
       }
     }
@@ -624,16 +635,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ts_w(T_S, T_Q + kk * 8, kslice(bk, kk), ID_KK, kk > 0);
       };
-      auto issue_dp = [=](int st) {  // dP = dO V^T  (dO from shared memory)
-        const uint64_t bv = kdesc0(sbase + OFF_V + st * TILE_BYTES);
+      auto issue_dp = [=](int sv) {  // dP = dO V^T  (dO from shared memory)
+        const uint64_t bv = kdesc0(sbase + OFF_V + sv * TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_DP, kslice(dDO0, kk), kslice(bv, kk), ID_KK, kk > 0);
       };
       auto wait_kv = [&](uint32_t k_it) -> bool {
-        const int st = k_it % KSTAGE;
-        const uint32_t ph = (k_it / KSTAGE) & 1;
-        if (!mbar_wait_w(&bars->k_full[st], ph, wc, ST_BWD_WAIT | 0x14)) return false;
-        if (!mbar_wait_w(&bars->v_full[st], ph, wc, ST_BWD_WAIT | 0x15)) return false;
+        if (!mbar_wait_w(&bars->k_full[k_it % KSTAGE], (k_it / KSTAGE) & 1, wc, ST_BWD_WAIT | 0x14)) return false;
+        if (!mbar_wait_w(&bars->v_full[k_it % VSTAGE], (k_it / VSTAGE) & 1, wc, ST_BWD_WAIT | 0x15)) return false;
         return true;
       };
       // S for KV tile k_it once the previous S is in registers, then dP once the
@@ -654,8 +663,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         }
         first_dp = false;
         tc_fence_after();
-        issue_dp(k_it % KSTAGE);
+        issue_dp(k_it % VSTAGE);
         mma_commit_w(&bars->dp_full);
+        mma_commit_w(&bars->v_empty[k_it % VSTAGE]);   // V is done with once dP is computed
         return true;
       };
       for (int64_t r = 0; ok; ++r) {
@@ -683,7 +693,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           for (int kk = 0; kk < BT / 16; ++kk)   // dQ += dS K  (dS from TMEM, K MN-major)
             mma_ts_w(T_DQ, T_DS + pcol(kk), mnslice(mk, kk), ID_TM, (kk > 0) | (t > 0 ? 1u : 0u));
           mma_commit_w(&bars->ds_free);
-          mma_commit_w(&bars->kv_empty[st]);
+          mma_commit_w(&bars->k_empty[st]);
           if (t == T - 1) {
             mma_commit_w(&bars->do_empty);
             mma_commit_w(&bars->qo_empty);
