@@ -50,8 +50,8 @@ UNIT = "TFLOP/s"
 # source it was taken on: the hash of csrc/<file> at capture time.
 NCU_TRAFFIC = {
     "fwd": {"sha256": "4984ee29123d382ec59c34b8b8812d0820b11b7684c12a2957fa787a1feb7464", "workload": "long_128k", "bytes_per_launch": (10.408 + 1.132) * 1e9},
-    "bwd_dkv": {"sha256": "78cc7300f323f8d4c05ef6c0f7c4482dbeded4512a0b6134ae9b7729458c99e5", "workload": "long_128k", "bytes_per_launch": (10.146 + 2.278) * 1e9},
-    "bwd_dq": {"sha256": "78cc7300f323f8d4c05ef6c0f7c4482dbeded4512a0b6134ae9b7729458c99e5", "workload": "long_128k", "bytes_per_launch": (13.032 + 1.066) * 1e9},
+    "bwd_dkv": {"sha256": "7cd21247ef1da222b6bc31ca254f6808ade6c00752f17ff439172f58036aef0a", "workload": "long_128k", "bytes_per_launch": (11.574 + 2.290) * 1e9},
+    "bwd_dq": {"sha256": "7cd21247ef1da222b6bc31ca254f6808ade6c00752f17ff439172f58036aef0a", "workload": "long_128k", "bytes_per_launch": (8.189 + 1.067) * 1e9},
     "decode_split": {"sha256": "cc1673471a60b305918fea7128dd71985116d8cde5fac48687e1004268484946", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
 }
 
