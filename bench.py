@@ -10,9 +10,9 @@ Default workload: 131072 tokens, 32 heads of dim 128, 32 ring blocks of
 each) are larger than L2, so no flush is needed between steps.
 
 The `e2e` figure runs the same steps through the public API from pinned host
-memory: every step uploads its inputs and downloads every output, on a copy
-stream that overlaps the neighbouring steps' compute (device tensors
-double-buffered), as a training loop would prefetch.
+memory: every step uploads its inputs and downloads every output, on two copy
+streams (one per direction) that overlap the neighbouring steps' compute
+(device tensors double-buffered), as a training loop would prefetch.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas; the real multi-GPU ring exchange is not built), the
@@ -118,26 +118,28 @@ class ClockSampler:
 
 def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list) -> float:
     """End-to-end loop with the host<->device copies overlapped with compute,
-    as a training or serving loop prefetches: a copy stream moves step k+1's
-    inputs in and step k's results out while the compute stream runs step k;
-    device inputs and outputs are double-buffered (sets 0 and 1).  The first
-    upload and the last download are not hidden.
+    as a training or serving loop prefetches: one copy stream uploads step
+    k+1's inputs and another downloads step k's results (both directions of
+    the link at once) while the compute stream runs step k; device inputs and
+    outputs are double-buffered (sets 0 and 1).  The first upload and the
+    last download are not hidden.
 
     h2d_list(b) / d2h_list(b): [(dst, src)] copies for buffer set b;
     compute(b): one step on set b, on the current stream.
     Returns ms per step, CUDA events from the first upload to the last download."""
     import torch
-    cs = torch.cuda.Stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    cs.wait_stream(stream)
-    with torch.cuda.stream(cs):
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    with torch.cuda.stream(up):
         for dst, src in h2d_list(0):
             dst.copy_(src, non_blocking=True)
-        ev_in[0].record(cs)
+        ev_in[0].record(up)
     for k in range(steps):
         b = k % 2
         stream.wait_event(ev_in[b])
@@ -146,19 +148,21 @@ def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list) -> float:
         with torch.cuda.stream(stream):
             compute(b)
         ev_done[b].record(stream)
-        with torch.cuda.stream(cs):
-            if k + 1 < steps:
-                nb = (k + 1) % 2
+        if k + 1 < steps:
+            nb = (k + 1) % 2
+            with torch.cuda.stream(up):
                 if k >= 1:
-                    cs.wait_event(ev_done[nb])    # step k-1 no longer reads set nb
+                    up.wait_event(ev_done[nb])    # step k-1 no longer reads set nb
                 for dst, src in h2d_list(nb):
                     dst.copy_(src, non_blocking=True)
-                ev_in[nb].record(cs)
-            cs.wait_event(ev_done[b])
+                ev_in[nb].record(up)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
             for dst, src in d2h_list(b):
                 dst.copy_(src, non_blocking=True)
-            ev_out[b].record(cs)
-    stream.wait_stream(cs)
+            ev_out[b].record(down)
+    stream.wait_stream(up)
+    stream.wait_stream(down)
     end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
@@ -397,7 +401,7 @@ def run_ours(args, w):
         "roofline": roofline,
         "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": "overlapped with the neighbouring steps' compute on a copy stream; double-buffered"},
+                "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); double-buffered"},
         "kernels": kernels,
         "gpu_launches": len(ktimes),
         "clocks": clk.summary(),
@@ -759,7 +763,7 @@ def run_ffn(args, w):
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                 "d2h_bytes_per_step": yh.numel() * yh.element_size(), "steps": e2e_steps,
-                "copies": "overlapped with the neighbouring steps' compute on a copy stream; double-buffered"},
+                "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); double-buffered"},
         "kernels": kernels, "kernels_note": "per-kernel times from a second pass with events between launches",
         "blocks_per_step": nblocks,
         "gpu_launches": len(ktimes),
