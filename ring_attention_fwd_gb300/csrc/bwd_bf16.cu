@@ -428,13 +428,24 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const float* dvec = reinterpret_cast<const float*>(smem + OFF_DVEC + sd * VEC_BYTES) + 64 * grp;
           const int q0 = 64 * grp;
           float pv[64];
+          if (vis_lo <= q0) {   // every column of this thread visible: no mask in the hot loop
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-            pv[c] = q0 + c < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-            pv[c + 1] = q0 + c + 1 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-            pv[c + 2] = q0 + c + 2 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-            pv[c + 3] = q0 + c + 3 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+            for (int c = 0; c < 64; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+              pv[c] = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+              pv[c + 1] = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+              pv[c + 2] = hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+              pv[c + 3] = hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+              pv[c] = q0 + c < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+              pv[c + 1] = q0 + c + 1 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+              pv[c + 2] = q0 + c + 2 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+              pv[c + 3] = q0 + c + 3 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+            }
           }
           if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0xf))) break;
           dp_ph ^= 1;
@@ -763,13 +774,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&bars->s_free);
-          const bool masked = tile_masked(g, w.i, j, kt, w.r0);
           const int rk0 = kt * BT + 64 * grp;                // first key row handled here
+          if (!tile_masked(g, w.i, j, kt, w.r0)) {           // no mask in the hot loop
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            float pc = hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r));
-            if (masked && rk0 + c >= lim) pc = 0.f;
-            pv[c] = __float_as_uint(pc);
+            for (int c = 0; c < 64; ++c)
+              pv[c] = __float_as_uint(hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r)));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float pc = hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r));
+              pv[c] = __float_as_uint(rk0 + c >= lim ? 0.f : pc);
+            }
           }
           if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0x1f))) break;
           dp_ph ^= 1;
