@@ -302,9 +302,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int k = 0; k < BN; ++k)
               if (rk0 + k >= lim) sv[k] = -INFINITY;
           }
-          float mx = sv[0];
+          // Row max as 4 independent chains (one chain would be 127 dependent fmaxf).
+          float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-          for (int k = 1; k < BN; ++k) mx = fmaxf(mx, sv[k]);
+          for (int k = 4; k < BN; k += 4) {
+            mx0 = fmaxf(mx0, sv[k]);
+            mx1 = fmaxf(mx1, sv[k + 1]);
+            mx2 = fmaxf(mx2, sv[k + 2]);
+            mx3 = fmaxf(mx3, sv[k + 3]);
+          }
+          const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
           // Rescale only when the max grew by more than the threshold: O and
           // l then share a stale reference max, which cancels in O / l.
           const float mt = mx * sl2;
