@@ -28,15 +28,16 @@
 //                   its own TMEM region; dQ += dS K accumulates in TMEM.  S
 //                   and dP are released as soon as they are in registers, so
 //                   the next tile's S and dP MMAs overlap this tile's work.
-// Every MMA is 128 wide (an MMA instruction costs ~93 clocks at any size on
-// this part, so wide ones keep the tensor pipe fed).  Overlap: the elementwise
-// warps release S as soon as it is in registers, so the next tile's S MMA runs
-// while they compute; P^T/dS^T go over dP, whose next write follows the MMAs
-// that read them.
-// Both main kernels: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
-// TMEM owner, warps 4-7 and 8-11 the elementwise work, one thread per TMEM lane
-// (row); warpgroup g owns columns [64g, 64g+64) and writes its packed bf16
-// results only over columns it has read.
+// Every MMA is 128 wide.  Overlap: the elementwise warps release S as soon as
+// it is in registers, so the next tile's S MMA runs while they compute;
+// P^T/dS^T go over dP, whose next write follows the MMAs that read them.
+// Both main kernels: warp 0 TMA producer (one thread), warp 1 MMA issuer and
+// TMEM owner (the whole warp runs the issue loop so its operands stay
+// warp-uniform; one elected lane issues each tcgen05 instruction -- a single
+// issuing thread in a divergent branch reaches only ~2/3 of the tensor rate
+// with 128-wide MMAs), warps 4-7 and 8-11 the elementwise work, one thread per
+// TMEM lane (row); warpgroup g owns columns [64g, 64g+64) and writes its
+// packed bf16 results only over columns it has read.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

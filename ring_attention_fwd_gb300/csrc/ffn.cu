@@ -21,8 +21,9 @@
 //
 // Kernel: persistent, one CTA per SM, 192 threads.  Warp 0 (one thread) loads
 // A and B K-chunks of 64 columns with TMA into a 4-stage ring (48 KB a stage,
-// 128-byte swizzle); warp 1 (one thread) issues tcgen05.mma M=128 N=256 K=16
-// into one of two TMEM accumulators (256 columns each) and commits; warps 2-5
+// 128-byte swizzle); warp 1 (the whole warp, one elected lane issuing) issues
+// tcgen05.mma M=128 N=256 K=16 into one of two TMEM accumulators (256 columns
+// each) and commits; warps 2-5
 // drain the other accumulator (one thread per row) while the next tile's
 // MMAs run.  Tiles are handed out dynamically (an atomic counter per launch,
 // taken by the TMA thread and passed to the MMA and epilogue warps through a
@@ -108,7 +109,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     mbar_init(&bars->drain, 1);
     for (int s = 0; s < TSLOTS; ++s) {
       mbar_init(&bars->tid_full[s], 1);
-      mbar_init(&bars->tid_empty[s], 1 + 128);   // the MMA thread and the 128 epilogue threads
+      mbar_init(&bars->tid_empty[s], 1 + 128);   // one lane of the MMA warp and the 128 epilogue threads
     }
     bars->abort = 0;
     fence_mbar_init();

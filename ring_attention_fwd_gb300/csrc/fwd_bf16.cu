@@ -13,9 +13,11 @@
 // tiles Q0, Q1) of one head inside one query block.  Roles:
 //   warp 0      TMA producer: Q0/Q1 once per unit, then K_j / V_j tiles into
 //               a 2-stage ring of shared-memory buffers.
-//   warp 1      MMA issuer (one thread): S_q = Q_q K^T (SS, both K-major)
-//               and O_q += P_q V (A = P from TMEM, B = V MN-major); the
-//               whole warp allocates and releases the 512 TMEM columns.
+//   warp 1      MMA issuer: S_q = Q_q K^T (SS, both K-major) and
+//               O_q += P_q V (A = P from TMEM, B = V MN-major).  The whole
+//               warp runs the issue loop (operands stay warp-uniform) and one
+//               elected lane issues each tcgen05 instruction; the warp also
+//               allocates and releases the 512 TMEM columns.
 //   warps 2-5   softmax for Q0, warps 6-9 softmax for Q1: one thread per
 //               row; load S from TMEM, mask, row max, exp2, row sum, write P
 //               (bf16) back over S, rescale O in TMEM when the max grew by
