@@ -154,7 +154,7 @@ struct Bars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[QSTAGE], q_empty[QSTAGE];
   uint64_t do_full[DSTAGE], do_empty[DSTAGE];
-  uint64_t s_full, s_free, dp_full, p_full, dkv_full, dkv_empty, drain;
+  uint64_t s_full, dp_full, p_full, ds_full, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -189,11 +189,10 @@ __device__ __forceinline__ int unit_steps(const RingGeom& g, int j, int kt) {
   }
   return T;
 }
-// Packed bf16 columns of the 16-query K-slice kk of P^T / dS^T inside the dP^T
-// region: warpgroup g (queries [64g, 64g+64)) packs P^T at [64g, 64g+32) and
-// dS^T at [64g+32, 64g+64).
-__device__ __forceinline__ uint32_t pcol_p(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
-__device__ __forceinline__ uint32_t pcol_ds(int kk) { return 64 * (kk >> 2) + 32 + 8 * (kk & 3); }
+// Packed bf16 column of the 16-query K-slice kk of P^T (inside the S^T region)
+// and of dS^T (inside the dP^T region): warpgroup g (queries [64g, 64g+64))
+// packs its values at [64g, 64g+32) of the region it has just read.
+__device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
 
 __global__ void __launch_bounds__(THREADS, 1)
 dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -220,9 +219,9 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_empty, 256);
     mbar_init(&bars->drain, 1);
@@ -308,8 +307,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       constexpr uint32_t ID_KK = idesc_bf16_f32(BT, BT, 0, 0);   // A, B K-major, N = 128
       constexpr uint32_t ID_TM = idesc_bf16_f32(BT, HD, 0, 1);   // A from TMEM, B MN-major
       const uint64_t dK0 = kdesc0(sbase + OFF_K), dV0 = kdesc0(sbase + OFF_V);
-      uint32_t it = 0, kv_ph = 0, sf_ph = 0, pf_ph = 0, dkve_ph = 0;
-      bool ok = true, first_unit = true, first_s = true;
+      uint32_t it = 0, kv_ph = 0, pf_ph = 0, dsf_ph = 0, dkve_ph = 0;
+      bool ok = true, first_unit = true;
       auto issue_s = [=](int st) {   // S^T = K Q^T
         const uint64_t bq = kdesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
@@ -320,6 +319,11 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_DP, kslice(dV0, kk), kslice(bdo, kk), ID_KK, kk > 0);
       };
+      // Per tile the tensor pipe runs dV(t), S^T(t+1), dK(t), dP^T(t+1).  The
+      // S region holds S^T(t), then P^T(t) (written by the elementwise warps),
+      // read by dV(t); S^T(t+1) is issued after dV(t), so it overwrites P^T only
+      // once it has been read.  Likewise the dP^T region: dP^T(t), dS^T(t),
+      // read by dK(t), then dP^T(t+1).
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
         if (u >= p.num_units) break;
@@ -329,29 +333,16 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (!(ok = mbar_wait_w(&bars->kv_full, kv_ph, wc, ST_BWD_WAIT | 3))) break;
         kv_ph ^= 1;
         if (!(ok = mbar_wait_w(&bars->q_full[it % QSTAGE], (it / QSTAGE) & 1, wc, ST_BWD_WAIT | 4))) break;
-        if (!first_s) {   // S^T region: the previous tile's S^T must have been read
-          if (!(ok = mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
-          sf_ph ^= 1;
-        }
-        first_s = false;
         tc_fence_after();
-        issue_s(it % QSTAGE);
+        issue_s(it % QSTAGE);    // S region: last read by the previous tile's dV MMAs
         mma_commit_w(&bars->s_full);
         if (!(ok = mbar_wait_w(&bars->do_full[it % DSTAGE], (it / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
         tc_fence_after();
-        issue_dp(it % DSTAGE);   // dP^T region: last read by the previous tile's dV / dK MMAs
+        issue_dp(it % DSTAGE);   // dP^T region: last read by the previous tile's dK MMAs
         mma_commit_w(&bars->dp_full);
         for (int t = 0; t < T && ok; ++t, ++it) {
           const int st = it % QSTAGE, sd = it % DSTAGE;
           const int nst = (it + 1) % QSTAGE, nsd = (it + 1) % DSTAGE;
-          if (t + 1 < T) {   // next tile's S^T as soon as this tile's S^T is in registers
-            if (!(ok = mbar_wait_w(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
-            if (!(ok = mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0xd))) break;
-            sf_ph ^= 1;
-            tc_fence_after();
-            issue_s(nst);
-            mma_commit_w(&bars->s_full);
-          }
           if (!(ok = mbar_wait_w(&bars->p_full, pf_ph, wc, ST_BWD_WAIT | 5))) break;
           pf_ph ^= 1;
           if (t == 0 && !first_unit) {
@@ -362,13 +353,22 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const uint32_t acc = t > 0 ? 1u : 0u;
           const uint64_t mdo = mndesc0(sbase + OFF_DO + sd * TILE_BYTES), mq = mndesc0(sbase + OFF_Q + st * TILE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO
-            mma_ts_w(T_DV, T_DP + pcol_p(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
-          mma_commit_w(&bars->do_empty[sd]);
+          for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO  (P^T in the S region)
+            mma_ts_w(T_DV, T_S + pcol(kk), mnslice(mdo, kk), ID_TM, (kk > 0) | acc);
+          if (t + 1 < T) {   // next tile's S^T, behind the dV MMAs that read P^T
+            if (!(ok = mbar_wait_w(&bars->q_full[nst], ((it + 1) / QSTAGE) & 1, wc, ST_BWD_WAIT | 0xa))) break;
+            tc_fence_after();
+            issue_s(nst);
+            mma_commit_w(&bars->s_full);
+          }
+          if (!(ok = mbar_wait_w(&bars->ds_full, dsf_ph, wc, ST_BWD_WAIT | 0x10))) break;
+          dsf_ph ^= 1;
+          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q
-            mma_ts_w(T_DK, T_DP + pcol_ds(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
+          for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q  (dS^T in the dP^T region)
+            mma_ts_w(T_DK, T_DP + pcol(kk), mnslice(mq, kk), ID_TM, (kk > 0) | acc);
           mma_commit_w(&bars->q_empty[st]);
+          mma_commit_w(&bars->do_empty[sd]);   // the dO slot holds D_vec, read until dS^T was stored
           if (t + 1 < T) {
             if (!(ok = mbar_wait_w(&bars->do_full[nsd], ((it + 1) / DSTAGE) & 1, wc, ST_BWD_WAIT | 0xc))) break;
             tc_fence_after();
@@ -418,9 +418,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           tmem_ld32(tS, sv);
           tmem_ld32(tS + 32, sv + 32);
           tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&bars->s_free);
-          // P^T while the previous tile's dV / dK and this tile's dP^T run.
+          // P^T while the previous tile's dK and this tile's dP^T run; it goes
+          // over this group's own S^T columns, so dV can start at once.
           // Query column q of the tile is visible to this key row iff q >= vis_lo.
           int vis_lo = 0;
           if (!key_ok) vis_lo = BT;
@@ -448,6 +447,16 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               pv[c + 3] = q0 + c + 3 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
             }
           }
+          {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) pk[c >> 1] = pack_bf16x2(pv[c], pv[c + 1]);
+            tmem_st16(tS, pk);
+            tmem_st16(tS + 16, pk + 16);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full);
           if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0xf))) break;
           dp_ph ^= 1;
           tc_fence_after();
@@ -455,23 +464,20 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           tmem_ld32(tDP, dpv);
           tmem_ld32(tDP + 32, dpv + 32);
           tmem_ld_wait();
+          {
+            uint32_t dk[32];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[16], dk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const int c = hh * 32 + k;
+            for (int c = 0; c < 64; c += 2) {
               const float2 d2 = *reinterpret_cast<const float2*>(dvec + c);
-              pk[k >> 1] = pack_bf16x2(pv[c], pv[c + 1]);
-              dk[k >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[c]) - d2.x),
+              dk[c >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[c]) - d2.x),
                                        pv[c + 1] * (__uint_as_float(dpv[c + 1]) - d2.y));
             }
-            tmem_st16(tDP + hh * 16, pk);        // P^T over this group's own dP^T columns
-            tmem_st16(tDP + 32 + hh * 16, dk);   // dS^T
+            tmem_st16(tDP, dk);            // dS^T over this group's own dP^T columns
+            tmem_st16(tDP + 16, dk + 16);
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&bars->p_full);
+          mbar_arrive(&bars->ds_full);
         }
       }
       if (!ok) break;
