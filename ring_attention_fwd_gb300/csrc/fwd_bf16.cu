@@ -39,26 +39,31 @@ namespace fwd {
 constexpr int BM = 128;        // rows per Q tile
 constexpr int BN = 128;        // rows per KV tile
 constexpr int HD = 128;        // head dim
-constexpr int NSTAGE = 2;
+// K tiles stream through a 3-stage ring and V tiles through a 2-stage one: a
+// K tile is done with once both S MMAs of its step are issued, a V tile only
+// after both PV MMAs, so K can be fetched further ahead.
+constexpr int KSTAGE = 3;
+constexpr int VSTAGE = 2;
 constexpr int THREADS = 320;
 constexpr uint32_t TILE_BYTES = BM * HD * 2;      // 32 KB (two 16 KB swizzled boxes)
 constexpr uint32_t BOX_BYTES = TILE_BYTES / 2;    // 128 rows x 64 cols
 constexpr uint32_t OFF_Q = 0;                      // Q0, Q1
-constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES; // K stages
-constexpr uint32_t OFF_V = OFF_K + NSTAGE * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + NSTAGE * TILE_BYTES;
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES; // KSTAGE tiles
+constexpr uint32_t OFF_V = OFF_K + KSTAGE * TILE_BYTES;  // VSTAGE tiles
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGE * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units: p <= 2^8 between rescales
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[NSTAGE], v_full[NSTAGE], kv_empty[NSTAGE];
+  uint64_t k_full[KSTAGE], k_empty[KSTAGE], v_full[VSTAGE], v_empty[VSTAGE];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Params {
@@ -100,10 +105,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < KSTAGE; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VSTAGE; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&bars->s_full[q], 1);
@@ -133,7 +141,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t kv_it = 0, qe_ph = 0, nq = 0;
+      uint32_t kv_it = 0, qe_ph = 0, nq = 0, nk = 0;
       bool ok = true;
       for (int64_t r = 0; ok; ++r) {
         const int64_t u = snake_pos(r, cta, grid);
@@ -157,17 +165,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (!block_visited(g, w.i, j)) continue;
           const int last = kt_last(g, w.i, j, w.r0);
           for (int kt = 0; kt <= last; ++kt) {
-            const int st = kv_it % NSTAGE;
-            const uint32_t ph = (kv_it / NSTAGE) & 1;
-            if (!(ok = mbar_wait(&bars->kv_empty[st], ph ^ 1, wc, ST_FWD_WAIT | 2))) break;
             const int krow = j * g.c + kt * BN;
-            mbar_arrive_expect_tx(&bars->k_full[st], TILE_BYTES);
+            const int sk = kv_it % KSTAGE, sv = kv_it % VSTAGE;
+            if (!(ok = mbar_wait(&bars->k_empty[sk], ((kv_it / KSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 2))) break;
+            mbar_arrive_expect_tx(&bars->k_full[sk], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_K + st * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[st],
+              tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk],
                           h * 64, krow, w.bh);
-            mbar_arrive_expect_tx(&bars->v_full[st], TILE_BYTES);
+            ++nk;
+            if (!(ok = mbar_wait(&bars->v_empty[sv], ((kv_it / VSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 11))) break;
+            mbar_arrive_expect_tx(&bars->v_full[sv], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_V + st * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[st],
+              tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv],
                           h * 64, krow, w.bh);
             ++kv_it;
           }
@@ -175,10 +184,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
       if (!ok) {
         // Let copies still in flight land before the CTA exits.
-        for (uint32_t k = (kv_it > NSTAGE ? kv_it - NSTAGE : 0); k < kv_it; ++k) {
-          mbar_drain(&bars->k_full[k % NSTAGE], (k / NSTAGE) & 1, 200000000ull);
-          mbar_drain(&bars->v_full[k % NSTAGE], (k / NSTAGE) & 1, 200000000ull);
-        }
+        for (uint32_t k = (nk > KSTAGE ? nk - KSTAGE : 0); k < nk; ++k)
+          mbar_drain(&bars->k_full[k % KSTAGE], (k / KSTAGE) & 1, 200000000ull);
+        for (uint32_t k = (kv_it > VSTAGE ? kv_it - VSTAGE : 0); k < kv_it; ++k)
+          mbar_drain(&bars->v_full[k % VSTAGE], (k / VSTAGE) & 1, 200000000ull);
         if (nq > 0) mbar_drain(&bars->q_full, (nq - 1) & 1, 200000000ull);
       }
     }
@@ -217,18 +226,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (!(ok = mbar_wait_w(&bars->q_full, q_ph, wc, ST_FWD_WAIT | 3))) break;
         q_ph ^= 1;
         {
-          const int st = kv_it % NSTAGE;
-          if (!(ok = mbar_wait_w(&bars->k_full[st], (kv_it / NSTAGE) & 1, wc, ST_FWD_WAIT | 4))) break;
+          const int sk = kv_it % KSTAGE;
+          if (!(ok = mbar_wait_w(&bars->k_full[sk], (kv_it / KSTAGE) & 1, wc, ST_FWD_WAIT | 4))) break;
           tc_fence_after();
-          issue_s(0, st);
-          issue_s(1, st);
+          issue_s(0, sk);
+          issue_s(1, sk);
+          mma_commit_w(&bars->k_empty[sk]);
         }
         for (int t = 0; t < T && ok; ++t, ++kv_it) {
-          const int st = kv_it % NSTAGE;
-          const uint32_t ph = (kv_it / NSTAGE) & 1;
-          const int nst = (kv_it + 1) % NSTAGE;
-          const uint32_t nph = ((kv_it + 1) / NSTAGE) & 1;
-          if (!(ok = mbar_wait_w(&bars->v_full[st], ph, wc, ST_FWD_WAIT | 5))) break;
+          const int sv = kv_it % VSTAGE;
+          const int nsk = (kv_it + 1) % KSTAGE;
+          const uint32_t nph = ((kv_it + 1) / KSTAGE) & 1;
+          if (!(ok = mbar_wait_w(&bars->v_full[sv], (kv_it / VSTAGE) & 1, wc, ST_FWD_WAIT | 5))) break;
           for (int q = 0; q < 2 && ok; ++q) {
             if (t == 0 && !first) {
               if (!(ok = mbar_wait_w(&bars->o_empty[q], oe_ph[q], wc, ST_FWD_WAIT | 6))) break;
@@ -237,17 +246,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!(ok = mbar_wait_w(&bars->p_full[q], pf_ph[q], wc, ST_FWD_WAIT | 7))) break;
             pf_ph[q] ^= 1;
             tc_fence_after();
-            issue_pv(q, st, t > 0 ? 1u : 0u);
-            if (q == 1) mma_commit_w(&bars->kv_empty[st]);
+            issue_pv(q, sv, t > 0 ? 1u : 0u);
+            if (q == 1) mma_commit_w(&bars->v_empty[sv]);
             if (t == T - 1) {
               if (q == 0) mma_commit_w(&bars->q_empty);
               mma_commit_w(&bars->o_full[q]);
             } else {
               if (q == 0) {
-                if (!(ok = mbar_wait_w(&bars->k_full[nst], nph, wc, ST_FWD_WAIT | 8))) break;
+                if (!(ok = mbar_wait_w(&bars->k_full[nsk], nph, wc, ST_FWD_WAIT | 8))) break;
                 tc_fence_after();
               }
-              issue_s(q, nst);
+              issue_s(q, nsk);
+              if (q == 1) mma_commit_w(&bars->k_empty[nsk]);
             }
           }
         }
