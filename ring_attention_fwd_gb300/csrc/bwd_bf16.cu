@@ -18,9 +18,9 @@
 //                   in TMEM while the query tiles of blocks i = j, j+1, ...
 //                   (mod N) that see KV block j -- the hosts block j travels
 //                   to around the ring -- stream past.  Per query tile:
-//                   S^T = K Q^T, dP^T = V dO^T; P^T and dS^T (bf16) are packed
-//                   over dP^T in TMEM; dV += P^T dO and dK += dS^T Q read them
-//                   from there.
+//                   S^T = K Q^T, dP^T = V dO^T; P^T (bf16) is packed over
+//                   S^T and dS^T over dP^T in TMEM; dV += P^T dO and
+//                   dK += dS^T Q read them from there.
 //   3. dq_kernel    Query-stationary, visiting KV tiles in the forward's ring
 //                   order; Q sits in TMEM as an A operand, dO in shared
 //                   memory.  Per KV tile: S = Q K^T, dP = dO V^T; P is taken
@@ -236,8 +236,8 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // TMEM: dV [0,128) dK [128,256) S^T [256,384) dP^T [384,512); P^T and dS^T
-  // are packed (bf16) over dP^T once it has been read.
+  // TMEM: dV [0,128) dK [128,256) S^T [256,384) dP^T [384,512); P^T is packed
+  // (bf16) over S^T and dS^T over dP^T once each has been read.
   const uint32_t T_DV = tmem, T_DK = tmem + 128, T_S = tmem + 256, T_DP = tmem + 384;
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int grid = gridDim.x, cta = blockIdx.x;
