@@ -15,6 +15,14 @@ from ring_attention_fwd_gb300.inputs import as_float64, make_inputs
 # accumulation -> O <= 2e-2, LSE <= 1e-3; float32 workload <= 1e-4.
 TOL = {"bf16": dict(o=2e-2, lse=1e-3), "f32": dict(o=1e-4, lse=1e-4)}
 
+# Limits of the backward's whole-sequence identities, per head and column:
+# |sum_k dK| <= SUM_DK_LIMIT * ||dK||_2 and
+# |sum_k dV - sum_q dO| <= SUM_DV_LIMIT * sqrt(||dV||_2^2 + ||dO||_2^2).
+# tests/test_tolerance_derivation.py derives them from the bf16 rounding points
+# of the kernels (CPU only).
+SUM_DK_LIMIT = 5e-2
+SUM_DV_LIMIT = 1e-2
+
 
 def to_cuda(inp: dict) -> dict:
     return {k: v.cuda() for k, v in inp.items()}
@@ -52,6 +60,17 @@ def fwd_full_check(ra, inp: dict, N: int, causal: bool, layout: str, dtype: str)
     return eo, el
 
 
+def attention_rows_chunked(q, k, v, rows, N: int, causal: bool, layout: str, chunk: int = 64):
+    """``oracle.attention_rows`` over ``rows``, ``chunk`` rows per call, so that
+    the rows-by-S score matrix of a million-token sequence stays small."""
+    rows = np.asarray(rows, dtype=np.int64)
+    o = np.zeros((rows.size, q.shape[1]))
+    lse = np.zeros(rows.size)
+    for c0 in range(0, rows.size, chunk):
+        o[c0:c0 + chunk], lse[c0:c0 + chunk] = orc.attention_rows(q, k, v, rows[c0:c0 + chunk], N, causal, layout)
+    return o, lse
+
+
 def fwd_sampled_check(ra, inp: dict, N: int, causal: bool, layout: str, heads, n_random: int, seed: int):
     """Run the CUDA forward on the full workload; compare sampled rows of the
     given heads with the oracle's row-by-row definition.  Also checks that
@@ -69,7 +88,7 @@ def fwd_sampled_check(ra, inp: dict, N: int, causal: bool, layout: str, heads, n
         q = inp["q"][b, h].to(torch.float64).numpy()
         k = inp["k"][b, h].to(torch.float64).numpy()
         v = inp["v"][b, h].to(torch.float64).numpy()
-        ro, rl = orc.attention_rows(q, k, v, rows, N, causal, layout)
+        ro, rl = attention_rows_chunked(q, k, v, rows, N, causal, layout)
         go = o[b, h, torch.from_numpy(rows).cuda()].float().cpu().numpy()
         gl = lse[b, h, torch.from_numpy(rows).cuda()].cpu().numpy()
         eo = max(eo, max_err(go, ro))

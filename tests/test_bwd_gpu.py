@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle as orc
-from gpu_helpers import max_err, sample_rows, workload_inputs
+from gpu_helpers import SUM_DK_LIMIT, SUM_DV_LIMIT, TOL, fwd_sampled_check, max_err, sample_rows, workload_inputs
 from ring_attention_fwd_gb300.inputs import WORKLOADS, as_float64, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -102,7 +102,22 @@ def test_bwd_deterministic_dk_dv_and_workspace_reuse(ra):
     assert float((a[0].float() - b[0].float()).abs().max()) <= 1e-2
 
 
-def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only):
+def check_sum_identities(dk, dv, do, heads):
+    """Every row of P sums to 1 and every row of dS to 0, so for every head and
+    column  sum_k dK = 0  and  sum_k dV = sum_q dO  (each query sees at least
+    its own key).  Checked over all S keys, so every key block of the full-size
+    output takes part; the sums run in float64 on the device."""
+    for h in heads:
+        gk = dk[0, h].double()
+        gv = dv[0, h].double()
+        gd = do[0, h].double()
+        rk = gk.sum(0).abs() / gk.norm(dim=0).clamp_min(1e-30)
+        rv = (gv.sum(0) - gd.sum(0)).abs() / (gv.norm(dim=0) ** 2 + gd.norm(dim=0) ** 2).sqrt()
+        assert float(rk.max()) <= SUM_DK_LIMIT, f"sum_k dK head {h}: {float(rk.max()):.3e} of ||dK||"
+        assert float(rv.max()) <= SUM_DV_LIMIT, f"sum_k dV - sum_q dO head {h}: {float(rv.max()):.3e}"
+
+
+def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only, late_window=2048, n_random=96):
     inp = workload_inputs(w, with_grad=True)
     N, causal, layout = w["N"], w["causal"], w["layout"]
     B, H, S, D = inp["q"].shape
@@ -113,21 +128,23 @@ def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only):
     ra.check_device_status()
     for t in (dq, dk, dv):
         assert bool(torch.isfinite(t.float()).all())
+    check_sum_identities(dk, dv, dev["do"], range(H))
     del o, lse, dev
     for h in dq_heads:
-        rows = sample_rows(S, N, 96, 7 + h)
+        rows = sample_rows(S, N, n_random, 7 + h)
         q, k, v, do = (inp[x][0, h].to(torch.float64).numpy() for x in ("q", "k", "v", "do"))
-        ref = orc.attention_bwd_dq_rows(q, k, v, do, rows, N, causal, layout)
+        ref = np.concatenate([orc.attention_bwd_dq_rows(q, k, v, do, rows[c0:c0 + 64], N, causal, layout)
+                              for c0 in range(0, rows.size, 64)])
         _close(dq[0, h, torch.from_numpy(rows).cuda()].double().cpu().numpy(), ref, f"dQ rows head {h}")
     q, k, v, do = (inp[x][0, kv_head].to(torch.float64).numpy() for x in ("q", "k", "v", "do"))
     pos = orc.token_positions(S, N, layout)
     rng = np.random.default_rng(11)
-    if late_only:   # keys among the last 2048 tokens: only ~2048 queries see them
-        cand = np.nonzero(pos >= S - 2048)[0]
+    if late_only:   # keys among the last tokens: only that many queries see them
+        cand = np.nonzero(pos >= S - late_window)[0]
     else:
         cand = np.arange(S)
     keys = np.sort(rng.choice(cand, size=n_keys, replace=False))
-    rk, rv = orc.attention_bwd_kv_rows(q, k, v, do, keys, N, causal, layout)
+    rk, rv = orc.attention_bwd_kv_rows(q, k, v, do, keys, N, causal, layout, row_chunk=128)
     kidx = torch.from_numpy(keys).cuda()
     _close(dk[0, kv_head, kidx].double().cpu().numpy(), rk, "dK rows")
     _close(dv[0, kv_head, kidx].double().cpu().numpy(), rv, "dV rows")
@@ -144,3 +161,22 @@ def test_long_128k_workload_backward_sampled(ra):
     """The benchmark's workload and launch configuration: dQ on sampled rows of
     two heads, dK/dV on key rows among the last 2048 tokens of one head."""
     _sampled_bwd_check(ra, WORKLOADS["long_128k"], dq_heads=(0, 20), kv_head=9, n_keys=64, late_only=True)
+
+
+def test_million_token_forward_backward_sampled(ra):
+    """A 1,048,576-token causal sequence (2 heads of 128, 64 blocks of 16384
+    tokens): the lengths the method exists for.  Forward rows and dQ rows
+    sampled over the whole sequence and every block boundary, dK/dV on keys
+    among the last 1024 tokens, and the whole-sequence sum identities over all
+    keys of both heads."""
+    w = dict(B=1, H=2, S=1 << 20, D=128, N=64, causal=True, layout="contiguous", dtype="bf16", scale=0.5,
+             seed=8, grad=True)
+    inp = workload_inputs(w)
+    eo, el, _, _ = fwd_sampled_check(ra, {x: inp[x] for x in ("q", "k", "v")}, w["N"], True, "contiguous",
+                                     [(0, 0), (0, 1)], 32, 8)
+    assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
+    del inp
+    torch.cuda.empty_cache()
+    _sampled_bwd_check(ra, w, dq_heads=(1,), kv_head=0, n_keys=32, late_only=True, late_window=1024,
+                       n_random=16)
+
