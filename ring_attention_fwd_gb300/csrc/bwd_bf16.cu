@@ -116,8 +116,8 @@ struct Params {
   int64_t num_units;
   float scale_log2;  // log2(e) / sqrt(D)
   float inv_sqrt_d;
-  const float* lse2;   // [BH][N][n_mb][128]
-  const float* dvec;   // [BH][N][n_mb][128]
+  const float* nlse2;  // [BH][N][n_mb][128]: -LSE * log2(e)
+  const float* ndvec;  // [BH][N][n_mb][128]: -D_vec
   __nv_bfloat16* dQ;   // bf16 outputs (accumulate == 0)
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
@@ -134,7 +134,7 @@ __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int
 
 // ============================================================== dK, dV
 namespace kv {
-// Q tiles (with their lse2 rows) and dO tiles (with their D_vec rows) stream
+// Q tiles (with their -LSE*log2(e) rows) and dO tiles (with their -D_vec rows) stream
 // through separate rings.  Q is the first operand a tile needs (S^T) and the
 // last one it releases (dK), so it gets the deeper ring; dO is released after
 // dV, a tile earlier.
@@ -144,8 +144,8 @@ constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
 constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;               // QSTAGE tiles
 constexpr uint32_t OFF_DO = OFF_Q + QSTAGE * TILE_BYTES;     // DSTAGE tiles
-constexpr uint32_t OFF_LSE = OFF_DO + DSTAGE * TILE_BYTES;   // QSTAGE x lse2[128]
-constexpr uint32_t OFF_DVEC = OFF_LSE + QSTAGE * VEC_BYTES;  // DSTAGE x dvec[128]
+constexpr uint32_t OFF_LSE = OFF_DO + DSTAGE * TILE_BYTES;   // QSTAGE x nlse2[128]
+constexpr uint32_t OFF_DVEC = OFF_LSE + QSTAGE * VEC_BYTES;  // DSTAGE x ndvec[128]
 constexpr uint32_t OFF_BAR = OFF_DVEC + DSTAGE * VEC_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -278,7 +278,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             mbar_arrive_expect_tx(&bars->q_full[sq], TILE_BYTES + VEC_BYTES);
             for (int h = 0; h < 2; ++h)
               tma_load_3d(smem + OFF_Q + sq * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full[sq], h * 64, qrow, bh);
-            bulk_load(smem + OFF_LSE + sq * VEC_BYTES, p.lse2 + vrow, VEC_BYTES, &bars->q_full[sq]);
+            bulk_load(smem + OFF_LSE + sq * VEC_BYTES, p.nlse2 + vrow, VEC_BYTES, &bars->q_full[sq]);
             ++nq;
             const int sd = ndo % DSTAGE;
             if (!(ok = mbar_wait(&bars->do_empty[sd], ((ndo / DSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0xb))) break;
@@ -286,7 +286,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int h = 0; h < 2; ++h)
               tma_load_3d(smem + OFF_DO + sd * TILE_BYTES + h * BOX_BYTES, &tmDO, &bars->do_full[sd], h * 64, qrow,
                           bh);
-            bulk_load(smem + OFF_DVEC + sd * VEC_BYTES, p.dvec + vrow, VEC_BYTES, &bars->do_full[sd]);
+            bulk_load(smem + OFF_DVEC + sd * VEC_BYTES, p.ndvec + vrow, VEC_BYTES, &bars->do_full[sd]);
             ++ndo;
           }
         }
@@ -391,6 +391,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int t_row = quad * 32 + lane;                  // key row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
     uint32_t it = 0, s_ph = 0, dp_ph = 0, dkv_ph = 0;
     bool ok = true;
     for (int64_t r = 0; ok; ++r) {
@@ -424,28 +425,28 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           int vis_lo = 0;
           if (!key_ok) vis_lo = BT;
           else if (dpair && qt == kt) vis_lo = t_row + 1 - incl;
-          const float* lse2 = reinterpret_cast<const float*>(smem + OFF_LSE + st * VEC_BYTES) + 64 * grp;
-          const float* dvec = reinterpret_cast<const float*>(smem + OFF_DVEC + sd * VEC_BYTES) + 64 * grp;
+          const float* nlse2 = reinterpret_cast<const float*>(smem + OFF_LSE + st * VEC_BYTES) + 64 * grp;
+          const float* ndvec = reinterpret_cast<const float*>(smem + OFF_DVEC + sd * VEC_BYTES) + 64 * grp;
           const int q0 = 64 * grp;
           float pv[64];
-          if (vis_lo <= q0) {   // every column of this thread visible: no mask in the hot loop
+          // Exponent arguments two at a time (packed f32x2 FMA, each lane
+          // rounded as fmaf): s * log2(e)/sqrt(d) - LSE*log2(e).
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-              pv[c] = hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-              pv[c + 1] = hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-              pv[c + 2] = hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-              pv[c + 3] = hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
-            }
-          } else {
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
+            const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2v,
+                                          make_float2(l4.x, l4.y));
+            const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2v,
+                                          make_float2(l4.z, l4.w));
+            pv[c] = hw_exp2(a01.x);
+            pv[c + 1] = hw_exp2(a01.y);
+            pv[c + 2] = hw_exp2(a23.x);
+            pv[c + 3] = hw_exp2(a23.y);
+          }
+          if (vis_lo > q0) {   // some column of this thread hidden (diagonal or ragged tile)
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-              pv[c] = q0 + c < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-              pv[c + 1] = q0 + c + 1 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-              pv[c + 2] = q0 + c + 2 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-              pv[c + 3] = q0 + c + 3 < vis_lo ? 0.f : hw_exp2(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
-            }
+            for (int c = 0; c < 64; ++c)
+              if (q0 + c < vis_lo) pv[c] = 0.f;
           }
           {
             uint32_t pk[32];
@@ -467,10 +468,12 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           {
             uint32_t dk[32];
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              const float2 d2 = *reinterpret_cast<const float2*>(dvec + c);
-              dk[c >> 1] = pack_bf16x2(pv[c] * (__uint_as_float(dpv[c]) - d2.x),
-                                       pv[c + 1] * (__uint_as_float(dpv[c + 1]) - d2.y));
+            for (int c = 0; c < 64; c += 2) {   // dS^T = P^T (dP^T - D_vec), two lanes at a time
+              const float2 nd2 = *reinterpret_cast<const float2*>(ndvec + c);
+              const float2 ds = __fmul2_rn(make_float2(pv[c], pv[c + 1]),
+                                           __fadd2_rn(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                                      nd2));
+              dk[c >> 1] = pack_bf16x2(ds.x, ds.y);
             }
             tmem_st16(tDP, dk);            // dS^T over this group's own dP^T columns
             tmem_st16(tDP + 16, dk + 16);
@@ -730,6 +733,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     const int row = quad * 32 + lane;                    // query row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
     uint32_t s_ph = 0, dp_ph = 0, dsf_ph = 0, dq_ph = 0, qoe_ph = 0;
     bool ok = true, first_unit = true, first_ds = true;
     for (int64_t r = 0; ok; ++r) {
@@ -763,8 +767,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       tc_fence_before();
       mbar_arrive(&bars->qo_full);
       const int64_t vr = vec_row(g, w.bh, w.i, w.r0 / BT) + row;
-      const float lse2_r = p.lse2[vr];     // +inf past the block end: P = 0
-      const float dvec_r = p.dvec[vr];
+      const float nl = p.nlse2[vr];        // -inf past the block end: P = 0
+      const float2 nl2 = make_float2(nl, nl);
+      const float2 nd2 = make_float2(p.ndvec[vr], p.ndvec[vr]);
       for (int s = 0; s < g.N && ok; ++s) {
         const int j = ring_block(w.i, s, g.N);
         if (!block_visited(g, w.i, j)) continue;
@@ -782,16 +787,16 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           tc_fence_before();
           mbar_arrive(&bars->s_free);
           const int rk0 = kt * BT + 64 * grp;                // first key row handled here
-          if (!tile_masked(g, w.i, j, kt, w.r0)) {           // no mask in the hot loop
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {   // exponent arguments two at a time (packed f32x2 FMA)
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sl2v, nl2);
+            pv[c] = __float_as_uint(hw_exp2(a.x));
+            pv[c + 1] = __float_as_uint(hw_exp2(a.y));
+          }
+          if (tile_masked(g, w.i, j, kt, w.r0)) {            // diagonal or ragged tile only
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-              pv[c] = __float_as_uint(hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r)));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const float pc = hw_exp2(fmaf(__uint_as_float(pv[c]), sl2, -lse2_r));
-              pv[c] = __float_as_uint(rk0 + c >= lim ? 0.f : pc);
-            }
+              if (rk0 + c >= lim) pv[c] = 0u;
           }
           if (!(ok = mbar_wait(&bars->dp_full, dp_ph, wc, ST_BWD_WAIT | 0x1f))) break;
           dp_ph ^= 1;
@@ -804,9 +809,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           mbar_arrive(&bars->dp_free);
           uint32_t dk[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2)
-            dk[c >> 1] = pack_bf16x2(__uint_as_float(pv[c]) * (__uint_as_float(dpv[c]) - dvec_r),
-                                     __uint_as_float(pv[c + 1]) * (__uint_as_float(dpv[c + 1]) - dvec_r));
+          for (int c = 0; c < 64; c += 2) {   // dS = P (dP - D_vec), two lanes at a time
+            const float2 ds = __fmul2_rn(make_float2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                         __fadd2_rn(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                                    nd2));
+            dk[c >> 1] = pack_bf16x2(ds.x, ds.y);
+          }
           if (!first_ds) {   // the dS region: the previous tile's dQ MMAs must have read it
             if (!(ok = mbar_wait(&bars->ds_free, dsf_ph, wc, ST_BWD_WAIT | 0x20))) break;
             dsf_ph ^= 1;
@@ -842,11 +850,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
 }
 }  // namespace q
 
-// One warp per padded query row: D_vec = sum_d dO*O and lse2 = LSE*log2(e)
-// (D_vec = 0, lse2 = +inf for rows past the block end or with LSE = -inf).
+// One warp per padded query row: writes -D_vec = -sum_d dO*O and -LSE*log2(e)
+// (0 and -inf for rows past the block end or with LSE = -inf), negated so the
+// main kernels add them with packed f32x2 FMAs and adds.
 __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LSE,
-                                                   float* lse2, float* dvec, RingGeom g, int S, int64_t rows) {
+                                                   float* nlse2, float* ndvec, RingGeom g, int S, int64_t rows) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
@@ -857,7 +866,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restri
   const int i = static_cast<int>(t2 % g.N);
   const int64_t bh = t2 / g.N;
   const int lr = qt * BT + r;
-  float dv = 0.f, l2 = INFINITY;
+  float dv = 0.f, l2 = INFINITY;   // D_vec and LSE*log2(e)
   if (lr < g.c) {
     const int64_t row = bh * S + static_cast<int64_t>(i) * g.c + lr;
     const uint2 a = *reinterpret_cast<const uint2*>(O + row * HD + lane * 4);
@@ -879,8 +888,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restri
     l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
   }
   if (lane == 0) {
-    lse2[w] = l2;
-    dvec[w] = dv;
+    nlse2[w] = -l2;
+    ndvec[w] = -dv;
   }
 }
 
@@ -902,8 +911,8 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.S = static_cast<int>(a.S);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
   p.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a.D)));
-  p.lse2 = a.lse2;
-  p.dvec = a.dvec;
+  p.nlse2 = a.nlse2;
+  p.ndvec = a.ndvec;
   p.accumulate = a.accumulate;
   p.dQ = a.accumulate ? nullptr : static_cast<__nv_bfloat16*>(a.dQ);
   p.dK = a.accumulate ? nullptr : static_cast<__nv_bfloat16*>(a.dK);
@@ -920,7 +929,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   const int64_t prow = a.B * a.H * a.N * p.g.n_mb * BT;   // padded query rows
   if (a.ev) cudaEventRecord(a.ev[0], a.stream);
   prep_kernel<<<static_cast<unsigned>((prow * 32 + 255) / 256), 256, 0, a.stream>>>(
-      static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.LSE, a.lse2, a.dvec, p.g,
+      static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.LSE, a.nlse2, a.ndvec, p.g,
       p.S, prow);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -167,8 +167,8 @@ struct BwdArgs {
   void* dQ;        // bf16 outputs, or f32 accumulators when `accumulate`
   void* dK;
   void* dV;
-  float* lse2;     // [B,H,N,ceil(c/128),128] float32 workspace: LSE * log2(e)
-  float* dvec;     // same layout: rowsum(dO * O)
+  float* nlse2;    // [B,H,N,ceil(c/128),128] float32 workspace: -LSE * log2(e)
+  float* ndvec;    // same layout: -rowsum(dO * O)
   int64_t B, H, S, D, N;
   int causal, striped;
   int strict;      // see RingGeom::strict (0 for whole-sequence calls)

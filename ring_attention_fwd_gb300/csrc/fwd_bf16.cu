@@ -64,7 +64,6 @@ struct Bars {
   int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Params {
   RingGeom g;
@@ -276,6 +275,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const uint32_t tS = tmem + lane_off + q * 128;
     const uint32_t tO = tmem + lane_off + 256 + q * 128;
     const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
     uint32_t s_ph = 0, o_ph = 0;
     bool ok = true;
     for (int64_t r = 0; ok; ++r) {
@@ -314,14 +314,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             for (int k = 0; k < BN; ++k)
               if (rk0 + k >= lim) sv[k] = -INFINITY;
           }
-          // Row max as 4 independent chains (one chain would be 127 dependent fmaxf).
-          float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+          // Row max as 4 independent chains of three-input maxima (two new
+          // values per instruction).
+          float mx0 = fmaxf(sv[0], sv[4]), mx1 = fmaxf(sv[1], sv[5]), mx2 = fmaxf(sv[2], sv[6]),
+                mx3 = fmaxf(sv[3], sv[7]);
 #pragma unroll
-          for (int k = 4; k < BN; k += 4) {
-            mx0 = fmaxf(mx0, sv[k]);
-            mx1 = fmaxf(mx1, sv[k + 1]);
-            mx2 = fmaxf(mx2, sv[k + 2]);
-            mx3 = fmaxf(mx3, sv[k + 3]);
+          for (int k = 8; k < BN; k += 8) {
+            mx0 = fmax3(mx0, sv[k], sv[k + 4]);
+            mx1 = fmax3(mx1, sv[k + 1], sv[k + 5]);
+            mx2 = fmax3(mx2, sv[k + 2], sv[k + 6]);
+            mx3 = fmax3(mx3, sv[k + 3], sv[k + 7]);
           }
           const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
           // Rescale only when the max grew by more than the threshold: O and
@@ -336,20 +338,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           }
           const bool rescale_o = (t > 0) && __any_sync(0xffffffffu, grow);
           const float mref = (m_use == -INFINITY) ? 0.f : m_use;
-          float rs = 0.f;
+          const float2 nm2 = make_float2(-mref, -mref);
+          // Exponent arguments and the row sum two lanes at a time (packed
+          // f32x2 FMA and add): the sum runs as an even and an odd chain.
+          float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             uint32_t pk[16];
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
-              const float p0 = hw_exp2(fmaf(sv[ch * 32 + k], sl2, -mref));
-              const float p1 = hw_exp2(fmaf(sv[ch * 32 + k + 1], sl2, -mref));
-              rs += p0 + p1;
-              pk[k >> 1] = pack_bf16x2(p0, p1);
+              const float2 a = __ffma2_rn(make_float2(sv[ch * 32 + k], sv[ch * 32 + k + 1]), sl2v, nm2);
+              const float2 pp = make_float2(hw_exp2(a.x), hw_exp2(a.y));
+              rs2 = __fadd2_rn(rs2, pp);
+              pk[k >> 1] = pack_bf16x2(pp.x, pp.y);
             }
             tmem_st16(tS + ch * 16, pk);
           }
-          l += rs;
+          l += rs2.x + rs2.y;
           if (rescale_o) {   // O_q is idle: PV_q(t-1) completed before S_q(t) was signalled
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -357,7 +362,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               tmem_ld32(tO + ch * 32, ov);
               tmem_ld_wait();
 #pragma unroll
-              for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+              for (int k = 0; k < 32; k += 2) {
+                const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ov[k]), __uint_as_float(ov[k + 1])),
+                                             make_float2(alpha, alpha));
+                ov[k] = __float_as_uint(o2.x);
+                ov[k + 1] = __float_as_uint(o2.y);
+              }
               tmem_st32(tO + ch * 32, ov);
             }
           }

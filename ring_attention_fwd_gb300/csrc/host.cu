@@ -421,8 +421,8 @@ int bwd_impl(const char* who, const void* Q, const void* K, const void* V, const
   ra::BwdArgs a;
   a.Q = Q; a.K = K; a.V = V; a.O = O; a.LSE = LSE; a.dO = dO;
   a.dQ = dQ; a.dK = dK; a.dV = dV;
-  a.lse2 = static_cast<float*>(workspace);
-  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.vec_bytes);
+  a.nlse2 = static_cast<float*>(workspace);
+  a.ndvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.vec_bytes);
   a.B = B; a.H = H; a.S = S; a.D = D; a.N = N;
   a.causal = causal;
   a.striped = layout == RA_STRIPED;

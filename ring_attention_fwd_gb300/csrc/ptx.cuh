@@ -269,6 +269,12 @@ __device__ __forceinline__ float hw_log2(float x) {
 }
 
 // Pack two floats into bf16x2 (round to nearest even); `lo` in bits 0..15.
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
