@@ -50,9 +50,9 @@ UNIT = "TFLOP/s"
 # code it was taken on: the hash of csrc/<file> without comments (_src_hash)
 # at capture time.
 NCU_TRAFFIC = {
-    "fwd": {"sha256": "473d7971bcf89e22671fa0b20c3b490606135bae701fb83ad3e88e2f4b0c9f1c", "workload": "long_128k", "bytes_per_launch": (14.539 + 1.134) * 1e9},
-    "bwd_dkv": {"sha256": "cc9cdb79a6a8720393dba12d48866eb3600a5882ad7c5127b103d5b972e4840f", "workload": "long_128k", "bytes_per_launch": (11.286 + 2.131) * 1e9},
-    "bwd_dq": {"sha256": "cc9cdb79a6a8720393dba12d48866eb3600a5882ad7c5127b103d5b972e4840f", "workload": "long_128k", "bytes_per_launch": (23.416 + 1.070) * 1e9},
+    "fwd": {"sha256": "4bed694e383aa80292ece1e1f98ed849fcee4680e9c257cf27ae65ed58f8f60d", "workload": "long_128k", "bytes_per_launch": (11.459 + 1.149) * 1e9},
+    "bwd_dkv": {"sha256": "80c11d931ea5f2610db86309b7a18290b038ce8ac0dbcf1632cdf29a85e09179", "workload": "long_128k", "bytes_per_launch": (15.016 + 2.134) * 1e9},
+    "bwd_dq": {"sha256": "80c11d931ea5f2610db86309b7a18290b038ce8ac0dbcf1632cdf29a85e09179", "workload": "long_128k", "bytes_per_launch": (10.887 + 1.066) * 1e9},
     "decode_split": {"sha256": "733ad39ef4633cbd9d703ea228e16e39d31daa93ce6adae96fedd2757bea1600", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
     "ffn_up": {"sha256": "aa92e7b87505de12e91fcef22a3f61e267b872092e1256658477a35c5218c8fe", "workload": "ffn_7b", "bytes_per_launch": (220.352 + 80.051) * 1e6},
 }
