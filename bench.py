@@ -174,6 +174,40 @@ def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list) -> float:
     return start.elapsed_time(end) / steps
 
 
+def link_times(stream, h2d, d2h) -> dict:
+    """One step's host<->device copies with no compute beside them: uploads
+    alone, downloads alone, and both directions at once (on two streams), so
+    an e2e figure can be read against what the host link allows.
+    h2d / d2h: [(dst, src)] copies.  Returns ms and GB/s."""
+    import torch
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(pairs_up, pairs_down):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
+            for dst, src in pairs_up:
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(down):
+            for dst, src in pairs_down:
+                dst.copy_(src, non_blocking=True)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1)
+
+    bu = sum(src.numel() * src.element_size() for _, src in h2d)
+    bd = sum(src.numel() * src.element_size() for _, src in d2h)
+    h_ms = min(timed(h2d, []) for _ in range(2))
+    d_ms = min(timed([], d2h) for _ in range(2))
+    b_ms = min(timed(h2d, d2h) for _ in range(2))
+    return {"h2d_ms": h_ms, "d2h_ms": d_ms, "both_ms": b_ms, "h2d_gbs": bu / h_ms / 1e6, "d2h_gbs": bd / d_ms / 1e6}
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -356,6 +390,7 @@ def run_ours(args, w):
     e2e_steps = max(8, args.steps)          # amortises the unhidden first upload and last download
     e2e_ms = pipelined_e2e(e2e_steps, stream, lambda b: [(ins[b][n], host[n]) for n in in_names], e2e_compute,
                            lambda b: [(outs_host[n], outs[b][n]) for n in outs_host])
+    link = link_times(stream, [(ins[1][n], host[n]) for n in in_names], [(outs_host[n], outs[0][n]) for n in outs_host])
     if ws > 1:
         tt = torch.tensor([e2e_ms], device="cuda")
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -407,7 +442,8 @@ def run_ours(args, w):
         "roofline": roofline,
         "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); double-buffered"},
+                "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); double-buffered",
+                "link_alone": link},
         "kernels": kernels,
         "gpu_launches": len(ktimes),
         "clocks": clk.summary(),

@@ -129,8 +129,8 @@ RA_API int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b
 
 /*
  * ra_bwd_workspace_bytes -- size of the caller-allocated workspace ra_bwd
- * needs for these sizes: per query row D_vec = rowsum(dO * O) and
- * LSE * log2(e), each stored per 128-row query tile of every block
+ * needs for these sizes: per query row -D_vec = -rowsum(dO * O) and
+ * -LSE * log2(e) (stored negated), each per 128-row query tile of every block
  * ([B,H,N,ceil(S/N/128),128] float32, 8 bytes per padded row in all), each
  * part 256-byte aligned.  Returns 0 on bad sizes (as ra_bwd would reject
  * them).
