@@ -1,7 +1,7 @@
 """Benchmark: ring-order blockwise attention forward + backward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k|decode_256k|ffn_7b]
+                    [--workload long_128k|fwdbwd_64k|balance_32k|causal_8k|long_1m|decode_256k|ffn_7b]
 
 A step is one pass of the whole path over one batch of synthetic input: the
 forward (O, LSE) followed by the backward (dQ, dK, dV) from the saved state.
@@ -17,6 +17,9 @@ streams (one per direction) that overlap the neighbouring steps' compute
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas; the real multi-GPU ring exchange is not built), the
 timing is the max over ranks and `value` sums the ranks' work.
+
+`--workload long_1m` runs the same step on 1,048,576 tokens (4 heads, 64 ring
+blocks of 16384).
 
 `--workload decode_256k` measures ring decode instead (one new token against
 a resident 256K-token KV cache; HBM-bound, reported in GB/s).
@@ -879,7 +882,8 @@ def main():
     if args.workload in DECODE_WORKLOADS:
         run_decode(args, dict(DECODE_WORKLOADS[args.workload]))
         return
-    w = dict(WORKLOADS[args.workload])
+    from ring_attention_fwd_gb300.inputs import LONG_WORKLOADS
+    w = dict(WORKLOADS[args.workload] if args.workload in WORKLOADS else LONG_WORKLOADS[args.workload])
     if args.impl == "reference":
         run_reference(args, w)
     else:

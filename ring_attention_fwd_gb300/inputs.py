@@ -67,6 +67,16 @@ WORKLOADS = {
 }
 
 
+# Beyond the specified workloads: a sequence in the million-token range the
+# method exists for (1,048,576 tokens in 64 ring blocks of 16384, 4 heads).
+# Same recipe; measured by `bench.py --workload long_1m`, and a 2-head copy is
+# the long-sequence parity case of the tests.
+LONG_WORKLOADS = {
+    "long_1m": dict(B=1, H=4, S=1 << 20, D=128, N=64, causal=True, layout="contiguous",
+                    dtype="bf16", scale=0.5, seed=8, grad=True),
+}
+
+
 def make_decode_inputs(B: int, H: int, S: int, D: int, seed: int, *, scale: float = 1.0) -> dict:
     """Return {'q' [B, H, D], 'k', 'v' [B, H, S, D]} bf16 CPU tensors for ring
     decode: one new query token per (b, h) and an S-row KV cache.

@@ -13,7 +13,7 @@ import torch
 
 import oracle as orc
 from gpu_helpers import SUM_DK_LIMIT, SUM_DV_LIMIT, TOL, fwd_sampled_check, max_err, sample_rows, workload_inputs
-from ring_attention_fwd_gb300.inputs import WORKLOADS, as_float64, make_inputs
+from ring_attention_fwd_gb300.inputs import LONG_WORKLOADS, WORKLOADS, as_float64, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -169,8 +169,7 @@ def test_million_token_forward_backward_sampled(ra):
     sampled over the whole sequence and every block boundary, dK/dV on keys
     among the last 1024 tokens, and the whole-sequence sum identities over all
     keys of both heads."""
-    w = dict(B=1, H=2, S=1 << 20, D=128, N=64, causal=True, layout="contiguous", dtype="bf16", scale=0.5,
-             seed=8, grad=True)
+    w = dict(LONG_WORKLOADS["long_1m"], H=2)
     inp = workload_inputs(w)
     eo, el, _, _ = fwd_sampled_check(ra, {x: inp[x] for x in ("q", "k", "v")}, w["N"], True, "contiguous",
                                      [(0, 0), (0, 1)], 32, 8)
