@@ -54,8 +54,8 @@ UNIT = "TFLOP/s"
 # at capture time.
 NCU_TRAFFIC = {
     "fwd": {"sha256": "4bed694e383aa80292ece1e1f98ed849fcee4680e9c257cf27ae65ed58f8f60d", "workload": "long_128k", "bytes_per_launch": (11.459 + 1.149) * 1e9},
-    "bwd_dkv": {"sha256": "80c11d931ea5f2610db86309b7a18290b038ce8ac0dbcf1632cdf29a85e09179", "workload": "long_128k", "bytes_per_launch": (15.016 + 2.134) * 1e9},
-    "bwd_dq": {"sha256": "80c11d931ea5f2610db86309b7a18290b038ce8ac0dbcf1632cdf29a85e09179", "workload": "long_128k", "bytes_per_launch": (10.887 + 1.066) * 1e9},
+    "bwd_dkv": {"sha256": "51b8a9c3afd46a7210f9429034cff339409540d7a52d010f160f4447f9822079", "workload": "long_128k", "bytes_per_launch": (12.606 + 2.138) * 1e9},
+    "bwd_dq": {"sha256": "51b8a9c3afd46a7210f9429034cff339409540d7a52d010f160f4447f9822079", "workload": "long_128k", "bytes_per_launch": (9.970 + 1.067) * 1e9},
     "decode_split": {"sha256": "733ad39ef4633cbd9d703ea228e16e39d31daa93ce6adae96fedd2757bea1600", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
     "ffn_up": {"sha256": "aa92e7b87505de12e91fcef22a3f61e267b872092e1256658477a35c5218c8fe", "workload": "ffn_7b", "bytes_per_launch": (220.352 + 80.051) * 1e6},
 }

@@ -661,15 +661,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) mma_ss_w(T_DP, kslice(dDO0, kk), kslice(bv, kk), ID_KK, kk > 0);
       };
-      auto wait_kv = [&](uint32_t k_it) -> bool {
-        if (!mbar_wait_w(&bars->k_full[k_it % KSTAGE], (k_it / KSTAGE) & 1, wc, ST_BWD_WAIT | 0x14)) return false;
-        if (!mbar_wait_w(&bars->v_full[k_it % VSTAGE], (k_it / VSTAGE) & 1, wc, ST_BWD_WAIT | 0x15)) return false;
-        return true;
-      };
-      // S for KV tile k_it once the previous S is in registers, then dP once the
-      // previous dP is in registers.
+      // S for KV tile k_it once its K tile has landed and the previous S is in
+      // registers, then dP once its V tile has landed and the previous dP is in
+      // registers.
       auto issue_tile = [&](uint32_t k_it) -> bool {
-        if (!wait_kv(k_it)) return false;
+        if (!mbar_wait_w(&bars->k_full[k_it % KSTAGE], (k_it / KSTAGE) & 1, wc, ST_BWD_WAIT | 0x14)) return false;
         if (!first_s) {
           if (!mbar_wait_w(&bars->s_free, sf_ph, wc, ST_BWD_WAIT | 0x1c)) return false;
           sf_ph ^= 1;
@@ -678,6 +674,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         tc_fence_after();
         issue_s(k_it % KSTAGE);
         mma_commit_w(&bars->s_full);
+        if (!mbar_wait_w(&bars->v_full[k_it % VSTAGE], (k_it / VSTAGE) & 1, wc, ST_BWD_WAIT | 0x15)) return false;
         if (!first_dp) {
           if (!mbar_wait_w(&bars->dp_free, df_ph, wc, ST_BWD_WAIT | 0x1d)) return false;
           df_ph ^= 1;
