@@ -10,9 +10,9 @@
 // dK = dS^T Q / sqrt(d).
 //
 // Three launches, no atomics (dQ, dK, dV are each written by one CTA):
-//   1. prep_kernel  D_vec and LSE*log2(e) per query row, stored per 128-row
-//                   query tile (rows past a block's end get D_vec = 0 and
-//                   +inf, so they drop out of P by themselves).
+//   1. prep_kernel  -D_vec and -LSE*log2(e) per query row, stored negated
+//                   per 128-row query tile (rows past a block's end get 0 and
+//                   -inf, so they drop out of P by themselves).
 //   2. dkv_kernel   KV-stationary.  A work unit is one 128-row KV tile of one
 //                   head, held in shared memory, with dK and dV accumulating
 //                   in TMEM while the query tiles of blocks i = j, j+1, ...
@@ -29,8 +29,10 @@
 //                   and dP are released as soon as they are in registers, so
 //                   the next tile's S and dP MMAs overlap this tile's work.
 // Every MMA is 128 wide.  Overlap: the elementwise warps release S as soon as
-// it is in registers, so the next tile's S MMA runs while they compute;
-// P^T/dS^T go over dP, whose next write follows the MMAs that read them.
+// it is in registers, so the next tile's S MMA runs while they compute; in the
+// dK/dV kernel P^T goes over S^T and dS^T over dP^T, and the next write into
+// each region follows the MMA that reads it.  The elementwise arithmetic runs
+// on pairs of values with packed f32x2 FMAs, adds and multiplies.
 // Both main kernels: warp 0 TMA producer (one thread), warp 1 MMA issuer and
 // TMEM owner (the whole warp runs the issue loop so its operands stay
 // warp-uniform; one elected lane issues each tcgen05 instruction -- a single

@@ -11,8 +11,9 @@
 //
 // One persistent CTA per SM.  A work unit is 256 query rows (two 128-row
 // tiles Q0, Q1) of one head inside one query block.  Roles:
-//   warp 0      TMA producer: Q0/Q1 once per unit, then K_j / V_j tiles into
-//               a 2-stage ring of shared-memory buffers.
+//   warp 0      TMA producer: Q0/Q1 once per unit, then K_j tiles into a
+//               3-stage and V_j tiles into a 2-stage ring of shared-memory
+//               buffers.
 //   warp 1      MMA issuer: S_q = Q_q K^T (SS, both K-major) and
 //               O_q += P_q V (A = P from TMEM, B = V MN-major).  The whole
 //               warp runs the issue loop (operands stay warp-uniform) and one
@@ -21,7 +22,8 @@
 //   warps 2-5   softmax for Q0, warps 6-9 softmax for Q1: one thread per
 //               row; load S from TMEM, mask, row max, exp2, row sum, write P
 //               (bf16) back over S, rescale O in TMEM when the max grew by
-//               more than 2^8, epilogue O/l and LSE.
+//               more than 2^8, epilogue O/l and LSE.  The arithmetic runs on
+//               pairs of scores (packed f32x2 FMA and add, three-input max).
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 // The MMA issue order S0 S1 | PV0 S0' | PV1 S1' | ... lets the tensor core
 // work on one tile while the other tile's softmax runs (ping-pong).
