@@ -13,6 +13,8 @@ The `e2e` figure runs the same steps through the public API from pinned host
 memory: every step uploads its inputs and downloads every output, on two copy
 streams (one per direction) that overlap the neighbouring steps' compute
 (device tensors double-buffered), as a training loop would prefetch.
+`e2e.link_alone` times one step's copies with nothing else running (each
+direction alone and both at once), the bound the host link sets on `e2e`.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas; the real multi-GPU ring exchange is not built), the
