@@ -353,7 +353,7 @@ def attention_bwd_dq_rows(q, k, v, do, rows, n_blocks: int, causal: bool, layout
 
 
 def attention_bwd_kv_rows(q, k, v, do, key_rows, n_blocks: int, causal: bool, layout: str,
-                          row_chunk: int = 512):
+                          row_chunk: int = 512, query_rows=None):
     """dK and dV of selected key rows of ONE head, from Q, K, V, dO alone.
 
     Every query row that can see one of the keys (all rows, or under the causal
@@ -361,6 +361,9 @@ def attention_bwd_kv_rows(q, k, v, do, key_rows, n_blocks: int, causal: bool, la
     its O and LSE recomputed from the definition (``attention_rows``); then
         dV(k) = sum_q P(q,k) dO(q),   dS(q,k) = P(q,k) (dO(q).v_k - D_vec(q)),
         dK(k) = sum_q dS(q,k) q / sqrt(D),   D_vec(q) = dO(q).O(q).
+    ``query_rows`` (storage rows) restricts both sums to those queries: the
+    parts over a partition of the rows add up to the whole, as dK_j and dV_j
+    accumulate one query block per ring round ([CH] §5.2).
     Returns (dK [len(key_rows), D], dV [len(key_rows), D]).
     """
     S, D = q.shape
@@ -370,6 +373,8 @@ def attention_bwd_kv_rows(q, k, v, do, key_rows, n_blocks: int, causal: bool, la
         q_rows = np.nonzero(pos >= pos[key_rows].min())[0]
     else:
         q_rows = np.arange(S)
+    if query_rows is not None:
+        q_rows = np.intersect1d(q_rows, np.asarray(query_rows, dtype=np.int64))
     dK = np.zeros((key_rows.size, D))
     dV = np.zeros((key_rows.size, D))
     kk, vk = k[key_rows], v[key_rows]

@@ -363,6 +363,32 @@ def test_kv_rows_match_full_backward():
             np.testing.assert_allclose(gv, dv[keys], atol=1e-13)
 
 
+def test_kv_rows_split_over_query_blocks_adds_up():
+    """dK_j and dV_j accumulate one query block per ring round ([CH] §5.2):
+    the parts over any partition of the query rows add up to the full
+    backward's rows, and queries that see none of the keys add nothing."""
+    rng = np.random.default_rng(21)
+    S, N, D = 60, 5, 8
+    c = S // N
+    q, k, v, do = (_rand(rng, S, D) for _ in range(4))
+    for layout in LAYOUTS:
+        o, lse = orc.attention_rows(q, k, v, np.arange(S), N, True, layout)
+        _, dk, dv = orc.attention_bwd_head(q, k, v, o, lse, do, N, True, layout)
+        keys = np.array([1, 14, 30, 59])
+        gk, gv = np.zeros((keys.size, D)), np.zeros((keys.size, D))
+        for i in rng.permutation(N):
+            pk, pv = orc.attention_bwd_kv_rows(q, k, v, do, keys, N, True, layout, row_chunk=5,
+                                               query_rows=np.arange(i * c, (i + 1) * c))
+            gk += pk
+            gv += pv
+        np.testing.assert_allclose(gk, dk[keys], atol=1e-13)
+        np.testing.assert_allclose(gv, dv[keys], atol=1e-13)
+    pos = orc.token_positions(S, N, "contiguous")
+    early = np.nonzero(pos < 30)[0]      # contiguous causal: these queries cannot see key 30 or 59
+    pk, pv = orc.attention_bwd_kv_rows(q, k, v, do, np.array([30, 59]), N, True, "contiguous", query_rows=early)
+    assert not pk.any() and not pv.any()
+
+
 # ------------------------------------------------------------- work per device
 def test_product_pair_counter_matches_oracle():
     from ring_attention_fwd_gb300 import flops
