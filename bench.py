@@ -829,29 +829,6 @@ def run_ffn(args, w):
         print(json.dumps(line), flush=True)
 
 
-def run_mma_probe(args):
-    """Clocks per tcgen05.mma instruction (M=128, K=16) by operand source and
-    width; prints one JSON line (the table behind the kernels' design)."""
-    import torch
-    import ring_attention_fwd_gb300 as ra
-    torch.cuda.set_device(0)
-    rows = []
-    cases = [(ts, n, 0, 0) for ts in (False, True) for n in (64, 128, 256)]
-    cases += [(ts, 128, k, 0) for ts in (False, True) for k in (8, 1)]
-    cases += [(False, 128, 8, v) for v in (1, 2, 4, 7, 2 | 8, 2 | 16, 7 | 8)]
-    cases += [(True, 128, 8, v) for v in (2 | 8, 2 | 16)]
-    cases += [(ts, n, k, 32 | v) for ts in (False, True) for n, k, v in ((64, 0, 0), (128, 0, 0), (128, 8, 7 | 8),
-                                                                          (128, 8, 2 | 16))]
-    for ts, n, k, v in cases:
-        ra.probe_mma(ts, n, 1000, k, v)                    # warm-up
-        clk = ra.probe_mma(ts, n, 16000, k, v)
-        ideal = 128 * n * 16 * 2 / 8192.0
-        rows.append({"a": "tmem" if ts else "smem", "n": n, "switch_every": k, "variant": v, "clk_per_mma": clk,
-                     "ideal_clk": ideal, "frac_of_tensor_rate": ideal / clk})
-    print(json.dumps({"probe": "tcgen05.mma kind::f16, M=128, K=16, one CTA per SM, same accumulator",
-                      "sms": torch.cuda.get_device_properties(0).multi_processor_count, "rows": rows}), flush=True)
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -861,17 +838,12 @@ def main():
     ap.add_argument("--workload", default="long_128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mma-probe", action="store_true",
-                    help="clocks per tcgen05.mma instruction by operand source and width (one JSON line)")
     ap.add_argument("--balance", action="store_true",
                     help="report per-virtual-host work and time, striped vs contiguous (default workload balance_32k)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from ring_attention_fwd_gb300.inputs import WORKLOADS
-    if args.mma_probe:
-        run_mma_probe(args)
-        return
     if args.balance:
         if args.workload == "long_128k" and "--workload" not in sys.argv:
             args.workload = "balance_32k"

@@ -56,7 +56,11 @@ typedef enum {
   RA_ERR_TIMEOUT = 4       /* a bounded device-side wait ran out           */
 } ra_status;
 
-typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+typedef enum {
+  RA_F32 = 0,
+  RA_BF16 = 1,
+  RA_F32_BF16 = 2   /* ra_merge only: float32 state O_a, bf16 partial O_b */
+} ra_dtype;
 typedef enum { RA_CONTIGUOUS = 0, RA_STRIPED = 1 } ra_layout;
 
 /*
@@ -120,6 +124,9 @@ RA_API int ra_fwd_step(const void* Q_i, const void* K_j, const void* V_j,
  *
  *   O_a : [rows, D] of `dtype` (in/out);   lse_a : [rows] float32 (in/out)
  *   O_b : [rows, D] of `dtype` (in);       lse_b : [rows] float32 (in)
+ *   dtype RA_F32_BF16: O_a float32, O_b bf16 -- a ring host keeps its running
+ *   output in float32 across the rounds and folds each round's bf16 partial
+ *   (from ra_fwd_step) into it, so the output is rounded once, not per round.
  *   rows >= 0 (0 is a no-op), D in 1..1024.  Pointers 4-byte aligned (O_* of
  *   bf16 may be 2-byte aligned).  O_a and O_b must not overlap unless equal.
  * Errors: RA_ERR_ARG, RA_ERR_CUDA.
@@ -338,28 +345,6 @@ RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
 RA_API int ra_set_wait_test(int enable);
 
 /*
- * ra_probe_mma -- tensor-core issue-rate probe (measurement aid, no
- * counterpart on the pages).  One CTA per SM issues `iters` tcgen05.mma
- * kind::f16 instructions (M = 128, N = n, K = 16, bf16 in, f32 accumulate)
- * back to back (eight K-slices of a 128-deep tile per loop trip) into one
- * TMEM accumulator, or alternating between two every `switch_every` MMAs
- * (0 = never; needs n <= 128), A from shared memory (a_from_tmem = 0) or
- * TMEM (1), B from shared memory, operands pseudo-random; *clk_per_mma
- * receives the mean SM clocks per instruction.  `variant` (0..63) adds, per
- * group of eight MMAs: bit 0 a run-time accumulate flag; bit 1 a commit to an
- * mbarrier; bit 2 a wait on a completed mbarrier plus a tcgen05 fence; bit 3
- * (with bit 1) a wait for the group issued two groups earlier; bit 4 (with
- * bit 1) a wait for the previous group; bit 5 issues from a whole warp (one
- * elected lane) instead of a single thread.  Synchronous on the legacy default
- * stream; allocates no device memory.
- * Errors: RA_ERR_ARG (n not a multiple of 16 in 16..256, iters outside
- * 1..10^7, switch_every < 0 or with n > 128, variant outside 0..63, null
- * pointer), RA_ERR_CUDA.
- */
-RA_API int ra_probe_mma(int a_from_tmem, int n, int iters, int switch_every, int variant,
-                        double* clk_per_mma);
-
-/*
  * ra_check_device_status -- synchronise `stream`, then read and clear the
  * library's device-side status word.  Returns RA_ERR_TIMEOUT if any kernel
  * launched since the previous check gave up a bounded wait (the kernel then
@@ -367,10 +352,39 @@ RA_API int ra_probe_mma(int a_from_tmem, int n, int iters, int switch_every, int
  */
 RA_API int ra_check_device_status(void* stream);
 
+/*
+ * ra_read_checks -- report of the bounds-checked build (no counterpart on the
+ * pages; it stands in for a memory checker).  libringattn_checked.so is built
+ * from the same sources with every global-memory index of the epilogues and
+ * of the merge, preprocess, decode and float32 kernels, and every TMA box
+ * start coordinate, checked against the extent of the tensor it addresses.
+ * A failed check skips that access (a skipped TMA copy makes its waiters time
+ * out, so the call also reports RA_ERR_TIMEOUT) and is counted here.
+ * Synchronises `stream`, copies the current device's record into *out and
+ * clears it.  events[0]: rows of the bf16 forward whose running maximum jumped
+ * past the rescale threshold after keys had been folded in (their O was
+ * rescaled); events[1]: rescale passes over O (one per warp and tile);
+ * events[2]: TMA boxes checked; events[3]: other accesses checked.
+ * violations: accesses found out of bounds; first_site / first_index /
+ * first_extent: where the first one was (site codes name kernel and access;
+ * a TMA index packs z<<40 | y<<16 | x).
+ * Errors: RA_ERR_UNSUPPORTED from the default build (libringattn.so), which
+ * checks nothing; RA_ERR_ARG (null out); RA_ERR_CUDA.
+ */
+typedef struct {
+  uint64_t events[8];
+  uint32_t violations;
+  uint32_t first_site;
+  int64_t first_index;
+  int64_t first_extent;
+} ra_check_report;
+RA_API int ra_read_checks(ra_check_report* out, void* stream);
+
 /* Message for the calling thread's most recent non-OK status ("" if none). */
 RA_API const char* ra_last_error(void);
 
-/* Library version string, e.g. "ringattn 0.1 sm_103a". */
+/* Library version string, e.g. "ringattn 0.2 sm_103a" ("... checked" for the
+ * bounds-checked build). */
 RA_API const char* ra_version(void);
 
 #ifdef __cplusplus

@@ -13,12 +13,15 @@ import threading
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libringattn.so")
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libringattn.so")
+_CHECKED_PATH = os.path.join(_HERE, "libringattn_checked.so")
 _lib = None
 _lock = threading.Lock()
+_loaded = {}        # path -> CDLL
 
 RA_OK, RA_ERR_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
-RA_F32, RA_BF16 = 0, 1
+RA_F32, RA_BF16, RA_F32_BF16 = 0, 1, 2
 RA_CONTIGUOUS, RA_STRIPED = 0, 1
 _LAYOUT = {"contiguous": RA_CONTIGUOUS, "striped": RA_STRIPED}
 _DTYPE = {torch.float32: RA_F32, torch.bfloat16: RA_BF16}
@@ -43,10 +46,10 @@ SIGNATURES = {
     "ra_ffn": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "ra_set_timing_buffer": (_int, [_vp, _sz]),
     "ra_check_device_status": (_int, [_vp]),
-    "ra_probe_mma": (_int, [_int, _int, _int, _int, _int, ctypes.POINTER(ctypes.c_double)]),
     "ra_set_kernel_timing": (_int, [_int]),
     "ra_set_wait_test": (_int, [_int]),
     "ra_kernel_times": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_int)]),
+    "ra_read_checks": (_int, [_vp, _vp]),
     "ra_last_error": (ctypes.c_char_p, []),
     "ra_version": (ctypes.c_char_p, []),
 }
@@ -58,24 +61,63 @@ class RingAttnError(RuntimeError):
         self.code = code
 
 
+def _load(path: str):
+    if path not in _loaded:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m ring_attention_fwd_gb300.build` "
+                "(there is no non-CUDA fallback)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _loaded[path] = L
+    return _loaded[path]
+
+
 def lib():
-    """Load libringattn.so (once).  Raises RuntimeError if it was not built."""
+    """The library every call goes through: libringattn.so unless
+    ``use_checked_build(True)`` selected the bounds-checked build.  Loaded on
+    first use; raises RuntimeError if it was not built."""
     global _lib
     if _lib is not None:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise RuntimeError(
-                    f"{_LIB_PATH} is missing: build it with `python -m ring_attention_fwd_gb300.build` "
-                    "(there is no non-CUDA fallback)")
-            L = ctypes.CDLL(_LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                f = getattr(L, name)
-                f.restype = res
-                f.argtypes = args
-            _lib = L
+            _lib = _load(_LIB_PATH)
     return _lib
+
+
+def use_checked_build(enable: bool = True):
+    """Route every later call through libringattn_checked.so (every global
+    index and TMA box checked against its extent, kernel events counted; see
+    ``read_checks``) or, with False, back through libringattn.so.  The two
+    libraries keep separate device state: buffers are plain device memory and
+    work with either."""
+    global _lib
+    with _lock:
+        _lib = _load(_CHECKED_PATH if enable else _LIB_PATH)
+
+
+class CheckReport(ctypes.Structure):
+    _fields_ = [("events", ctypes.c_uint64 * 8), ("violations", ctypes.c_uint32), ("first_site", ctypes.c_uint32),
+                ("first_index", ctypes.c_int64), ("first_extent", ctypes.c_int64)]
+
+
+CHECK_EVENTS = ("fwd_rescale_rows", "fwd_rescale_passes", "tma_boxes_checked", "accesses_checked")
+
+
+def read_checks(stream=None) -> dict:
+    """Synchronise and return (then clear) the checked build's record:
+    event counts, and the number and first site of out-of-bounds accesses.
+    Raises RingAttnError(RA_ERR_UNSUPPORTED) on the default build."""
+    r = CheckReport()
+    _check(lib().ra_read_checks(ctypes.addressof(r), _stream_ptr(stream)))
+    out = {name: int(r.events[k]) for k, name in enumerate(CHECK_EVENTS)}
+    out.update(violations=int(r.violations), first_site=hex(r.first_site), first_index=int(r.first_index),
+               first_extent=int(r.first_extent))
+    return out
 
 
 def _check(rc: int):
@@ -88,30 +130,46 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype=None):
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
+    """Check what the C ABI cannot: the kernels take sizes from q alone, so a
+    tensor of another shape, dtype or device would be read or written out of
+    its bounds."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _need_4d(q: torch.Tensor, name: str = "q"):
+    _need(q, name)
+    if q.dim() != 4:
+        raise ValueError(f"{name} must be [B, H, S, D], got shape {tuple(q.shape)}")
+    if q.dtype not in _DTYPE:
+        raise ValueError("dtype must be bfloat16 or float32")
+    return q.shape
 
 
 def fwd(q, k, v, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
         o=None, lse=None, stream=None):
     """Ring-order blockwise attention forward.  q, k, v: [B, H, S, D] CUDA
     tensors (bf16 or f32) in storage order.  Returns (o, lse)."""
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, name, q.dtype)
-    if q.dtype not in _DTYPE:
-        raise ValueError("dtype must be bfloat16 or float32")
-    B, H, S, D = q.shape
+    B, H, S, D = _need_4d(q)
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    _need(o, "o", q.dtype)
-    _need(lse, "lse", torch.float32)
+    _need(o, "o", q.dtype, q.shape, q.device)
+    _need(lse, "lse", torch.float32, (B, H, S), q.device)
     _check(lib().ra_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, S, D, int(n_blocks),
                         int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], o.data_ptr(), lse.data_ptr(),
                         _stream_ptr(stream)))
@@ -123,13 +181,15 @@ def fwd_step(q_i, k_j, v_j, n_blocks: int, i: int, j: int, causal: bool = True, 
     """One ring step of host i: its query block q_i [B, H, c, D] against KV
     block j (k_j, v_j of the same shape).  Returns the partial (o, lse) over
     block j's keys; chain the steps with merge()."""
-    for name, t in (("q_i", q_i), ("k_j", k_j), ("v_j", v_j)):
-        _need(t, name, q_i.dtype)
-    B, H, c, D = q_i.shape
+    B, H, c, D = _need_4d(q_i, "q_i")
+    for name, t in (("k_j", k_j), ("v_j", v_j)):
+        _need(t, name, q_i.dtype, q_i.shape, q_i.device)
     if o is None:
         o = torch.empty_like(q_i)
     if lse is None:
         lse = torch.empty((B, H, c), dtype=torch.float32, device=q_i.device)
+    _need(o, "o", q_i.dtype, q_i.shape, q_i.device)
+    _need(lse, "lse", torch.float32, (B, H, c), q_i.device)
     _check(lib().ra_fwd_step(q_i.data_ptr(), k_j.data_ptr(), v_j.data_ptr(), B, H, c, D, int(n_blocks), int(i),
                              int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype], o.data_ptr(),
                              lse.data_ptr(), _stream_ptr(stream)))
@@ -137,17 +197,22 @@ def fwd_step(q_i, k_j, v_j, n_blocks: int, i: int, j: int, causal: bool = True, 
 
 
 def merge(o_a, lse_a, o_b, lse_b, *, stream=None):
-    """In-place LogSumExp merge of (o_b, lse_b) into (o_a, lse_a)."""
+    """In-place LogSumExp merge of (o_b, lse_b) into (o_a, lse_a).  o_a and
+    o_b are both float32 or both bf16, or o_a float32 and o_b bf16 (a float32
+    running state folding bf16 partials)."""
     _need(o_a, "o_a")
-    _need(o_b, "o_b", o_a.dtype)
-    _need(lse_a, "lse_a", torch.float32)
-    _need(lse_b, "lse_b", torch.float32)
+    if o_a.dtype not in _DTYPE or o_a.dim() < 1:
+        raise ValueError("o_a must be a bfloat16 or float32 tensor [..., D]")
+    mixed = o_a.dtype == torch.float32 and o_b.dtype == torch.bfloat16
+    _need(o_b, "o_b", o_b.dtype if mixed else o_a.dtype, o_a.shape, o_a.device)
+    _need(lse_a, "lse_a", torch.float32, o_a.shape[:-1], o_a.device)
+    _need(lse_b, "lse_b", torch.float32, o_a.shape[:-1], o_a.device)
     D = o_a.shape[-1]
     rows = o_a.numel() // D if D else 0
     if lse_a.numel() != rows or lse_b.numel() != rows or o_b.numel() != o_a.numel():
         raise ValueError("shape mismatch")
     _check(lib().ra_merge(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(), lse_b.data_ptr(), rows, D,
-                          _DTYPE[o_a.dtype], _stream_ptr(stream)))
+                          RA_F32_BF16 if mixed else _DTYPE[o_a.dtype], _stream_ptr(stream)))
     return o_a, lse_a
 
 
@@ -155,19 +220,28 @@ def bwd_workspace_bytes(B, H, S, D, N) -> int:
     return int(lib().ra_bwd_workspace_bytes(B, H, S, D, N))
 
 
+def _bwd_args(q, k, v, o, lse, do, qname="q"):
+    """Shape, dtype and device checks shared by the backward entry points."""
+    B, H, S, D = _need_4d(q, qname)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    _need(lse, "lse", torch.float32, (B, H, S), q.device)
+    return B, H, S, D
+
+
 def bwd(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout: str = "contiguous", *,
         dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Backward from the saved (o, lse).  Returns (dq, dk, dv)."""
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        _need(t, name, q.dtype)
-    _need(lse, "lse", torch.float32)
-    B, H, S, D = q.shape
+    B, H, S, D = _bwd_args(q, k, v, o, lse, do)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, name, q.dtype, q.shape, q.device)
     need = bwd_workspace_bytes(B, H, S, D, int(n_blocks))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", device=q.device)
     _check(lib().ra_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D, int(n_blocks),
                         int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype], workspace.data_ptr(),
@@ -181,14 +255,12 @@ def bwd_step(q_i, k_j, v_j, o_i, lse_i, do_i, dq_i, dk_j, dv_j, n_blocks: int, i
     against KV block j into the float32 accumulators dq_i, dk_j, dv_j (in
     place).  q_i, o_i, do_i, k_j, v_j: [B, H, c, D] bf16; lse_i: block i's
     final [B, H, c] LSE.  Returns (dq_i, dk_j, dv_j)."""
-    for name, t in (("q_i", q_i), ("k_j", k_j), ("v_j", v_j), ("o_i", o_i), ("do_i", do_i)):
-        _need(t, name, q_i.dtype)
-    _need(lse_i, "lse_i", torch.float32)
+    B, H, c, D = _bwd_args(q_i, k_j, v_j, o_i, lse_i, do_i, "q_i")
     for name, t in (("dq_i", dq_i), ("dk_j", dk_j), ("dv_j", dv_j)):
-        _need(t, name, torch.float32)
-    B, H, c, D = q_i.shape
+        _need(t, name, torch.float32, q_i.shape, q_i.device)
     if workspace is None:
         workspace = torch.empty(bwd_workspace_bytes(B, H, c, D, 1), dtype=torch.uint8, device=q_i.device)
+    _need(workspace, "workspace", device=q_i.device)
     _check(lib().ra_bwd_step(q_i.data_ptr(), k_j.data_ptr(), v_j.data_ptr(), o_i.data_ptr(), lse_i.data_ptr(),
                              do_i.data_ptr(), dq_i.data_ptr(), dk_j.data_ptr(), dv_j.data_ptr(), B, H, c, D,
                              int(n_blocks), int(i), int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype],
@@ -204,13 +276,12 @@ def bwd_noalloc(q, k, v, o, lse, do, n_blocks: int, causal: bool = True, layout:
     problems raise RingAttnError).  The output tensors may be passed in, so a
     caller that cannot allocate can reuse its own buffers.  Concurrent calls on
     one device race on that array.  Returns (dq, dk, dv)."""
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        _need(t, name, q.dtype)
-    _need(lse, "lse", torch.float32)
-    B, H, S, D = q.shape
+    B, H, S, D = _bwd_args(q, k, v, o, lse, do)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, name, q.dtype, q.shape, q.device)
     _check(lib().ra_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                 do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S, D,
                                 int(n_blocks), int(bool(causal)), _LAYOUT[layout], _DTYPE[q.dtype],
@@ -231,8 +302,8 @@ def decode(q, k, v, n_blocks: int = 1, *, o=None, lse=None, workspace=None, stre
     is the per-host ring step (chain the results with merge()).
     Returns (o [B, H, D], lse [B, H] float32)."""
     _need(q, "q")
-    _need(k, "k", q.dtype)
-    _need(v, "v", q.dtype)
+    _need(k, "k", q.dtype, device=q.device)
+    _need(v, "v", q.dtype, device=q.device)
     if q.dtype not in _DTYPE:
         raise ValueError("dtype must be bfloat16 or float32")
     B, H, S, D = k.shape
@@ -242,8 +313,8 @@ def decode(q, k, v, n_blocks: int = 1, *, o=None, lse=None, workspace=None, stre
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _need(o, "o", q.dtype)
-    _need(lse, "lse", torch.float32)
+    _need(o, "o", q.dtype, (B, H, D), q.device)
+    _need(lse, "lse", torch.float32, (B, H), q.device)
     if workspace is None:
         need = decode_workspace_bytes(B, H, S, D, int(n_blocks))
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -263,7 +334,7 @@ def ffn(x, w1, w3, w2, block_rows: int, *, y=None, workspace=None, stream=None):
     x: [T, h]; w1, w3: [f, h]; w2: [h, f] (bf16 CUDA tensors).  Rows are
     processed ``block_rows`` at a time.  Returns y [T, h]."""
     for name, t in (("x", x), ("w1", w1), ("w3", w3), ("w2", w2)):
-        _need(t, name, x.dtype)
+        _need(t, name, x.dtype, device=x.device)
     if x.dtype not in _DTYPE:
         raise ValueError("dtype must be bfloat16 or float32")
     T, h = x.shape
@@ -271,7 +342,7 @@ def ffn(x, w1, w3, w2, block_rows: int, *, y=None, workspace=None, stream=None):
     if tuple(w1.shape) != (f, h) or tuple(w3.shape) != (f, h) or tuple(w2.shape) != (h, f):
         raise ValueError("w1, w3 must be [f, h] and w2 [h, f]")
     y = torch.empty_like(x) if y is None else y
-    _need(y, "y", x.dtype)
+    _need(y, "y", x.dtype, x.shape, x.device)
     if workspace is None:
         workspace = torch.empty(max(1, ffn_workspace_bytes(T, h, f, int(block_rows))), dtype=torch.uint8,
                                 device=x.device)
@@ -318,16 +389,6 @@ def _kernel_name(call: int, kernel: int) -> str:
     if call == 3:                                   # feedforward: up/down per block
         return "ffn_down" if kernel % 2 else "ffn_up"
     return KERNEL_NAMES.get((call, kernel), f"{call}.{kernel}")
-
-
-def probe_mma(a_from_tmem: bool, n: int, iters: int = 16000, switch_every: int = 0, variant: int = 0) -> float:
-    """Mean SM clocks per tcgen05.mma (M=128, N=n, K=16) issued back to back,
-    alternating two accumulators every ``switch_every`` MMAs if > 0, with the
-    per-group steps selected by ``variant`` (see ra_probe_mma)."""
-    out = ctypes.c_double(0.0)
-    _check(lib().ra_probe_mma(int(bool(a_from_tmem)), int(n), int(iters), int(switch_every), int(variant),
-                              ctypes.byref(out)))
-    return out.value
 
 
 def check_device_status(stream=None):

@@ -128,6 +128,9 @@ struct Params {
   float* dVf;
   int accumulate;
   unsigned int* status;
+  int64_t BH;          // heads (B*H)
+  int64_t vec_rows;    // rows of nlse2 / ndvec: BH * N * n_mb * 128
+  CheckRec* chk;
 };
 
 __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int qt) {
@@ -265,6 +268,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_arrive_expect_tx(&bars->kv_full, 2 * TILE_BYTES);
         const int krow = j * g.c + kt * BT;
         for (int h = 0; h < 2; ++h) {
+          if (!RA_CHECK_BOX(p.chk, SITE_DKV_TMA_KV, h * 64, krow, bh, HD, p.S, p.BH, 8)) continue;
           tma_load_3d(smem + OFF_K + h * BOX_BYTES, &tmK, &bars->kv_full, h * 64, krow, bh);
           tma_load_3d(smem + OFF_V + h * BOX_BYTES, &tmV, &bars->kv_full, h * 64, krow, bh);
         }
@@ -279,16 +283,21 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!(ok = mbar_wait(&bars->q_empty[sq], ((nq / QSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 2))) break;
             mbar_arrive_expect_tx(&bars->q_full[sq], TILE_BYTES + VEC_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_Q + sq * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full[sq], h * 64, qrow, bh);
-            bulk_load(smem + OFF_LSE + sq * VEC_BYTES, p.nlse2 + vrow, VEC_BYTES, &bars->q_full[sq]);
+              if (RA_CHECK_BOX(p.chk, SITE_DKV_TMA_Q, h * 64, qrow, bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_Q + sq * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full[sq], h * 64, qrow,
+                            bh);
+            if (RA_CHECK_RANGE(p.chk, SITE_DKV_VEC, vrow, BT, p.vec_rows))
+              bulk_load(smem + OFF_LSE + sq * VEC_BYTES, p.nlse2 + vrow, VEC_BYTES, &bars->q_full[sq]);
             ++nq;
             const int sd = ndo % DSTAGE;
             if (!(ok = mbar_wait(&bars->do_empty[sd], ((ndo / DSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0xb))) break;
             mbar_arrive_expect_tx(&bars->do_full[sd], TILE_BYTES + VEC_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_DO + sd * TILE_BYTES + h * BOX_BYTES, &tmDO, &bars->do_full[sd], h * 64, qrow,
-                          bh);
-            bulk_load(smem + OFF_DVEC + sd * VEC_BYTES, p.ndvec + vrow, VEC_BYTES, &bars->do_full[sd]);
+              if (RA_CHECK_BOX(p.chk, SITE_DKV_TMA_DO, h * 64, qrow, bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_DO + sd * TILE_BYTES + h * BOX_BYTES, &tmDO, &bars->do_full[sd], h * 64,
+                            qrow, bh);
+            if (RA_CHECK_RANGE(p.chk, SITE_DKV_VEC, vrow, BT, p.vec_rows))
+              bulk_load(smem + OFF_DVEC + sd * VEC_BYTES, p.ndvec + vrow, VEC_BYTES, &bars->do_full[sd]);
             ++ndo;
           }
         }
@@ -491,15 +500,16 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       dkv_ph ^= 1;
       tc_fence_after();
       const int64_t krow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(j) * g.c + lk;
+      const bool st_ok = key_ok && RA_CHECK_RANGE(p.chk, SITE_DKV_OUT, krow * HD, HD, p.BH * p.S * HD);
       if (p.accumulate) {
         if (grp == 0)
-          add_row_f32(T_DV + lane_off, p.dVf + krow * HD, 1.f, key_ok, HD);
+          add_row_f32(T_DV + lane_off, p.dVf + krow * HD, 1.f, st_ok, HD);
         else
-          add_row_f32(T_DK + lane_off, p.dKf + krow * HD, p.inv_sqrt_d, key_ok, HD);
+          add_row_f32(T_DK + lane_off, p.dKf + krow * HD, p.inv_sqrt_d, st_ok, HD);
       } else if (grp == 0) {
-        store_row_bf16(T_DV + lane_off, p.dV + krow * HD, 1.f, key_ok, HD);
+        store_row_bf16(T_DV + lane_off, p.dV + krow * HD, 1.f, st_ok, HD);
       } else {
-        store_row_bf16(T_DK + lane_off, p.dK + krow * HD, p.inv_sqrt_d, key_ok, HD);
+        store_row_bf16(T_DK + lane_off, p.dK + krow * HD, p.inv_sqrt_d, st_ok, HD);
       }
       tc_fence_before();
       mbar_arrive(&bars->dkv_empty);
@@ -612,7 +622,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         }
         mbar_arrive_expect_tx(&bars->do_full, TILE_BYTES);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(smem + OFF_DO + h * BOX_BYTES, &tmDO, &bars->do_full, h * 64, w.i * g.c + w.r0, w.bh);
+          if (RA_CHECK_BOX(p.chk, SITE_DQ_TMA_DO, h * 64, w.i * g.c + w.r0, w.bh, HD, p.S, p.BH, 8))
+            tma_load_3d(smem + OFF_DO + h * BOX_BYTES, &tmDO, &bars->do_full, h * 64, w.i * g.c + w.r0, w.bh);
         ++nd;
         for (int s = 0; s < g.N && ok; ++s) {
           const int j = ring_block(w.i, s, g.N);
@@ -624,13 +635,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
             if (!(ok = mbar_wait(&bars->k_empty[sk], ((nk / KSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x12))) break;
             mbar_arrive_expect_tx(&bars->k_full[sk], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk], h * 64, krow, w.bh);
+              if (RA_CHECK_BOX(p.chk, SITE_DQ_TMA_K, h * 64, krow, w.bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk], h * 64, krow,
+                            w.bh);
             ++nk;
             const int sv = nv % VSTAGE;
             if (!(ok = mbar_wait(&bars->v_empty[sv], ((nv / VSTAGE) & 1) ^ 1, wc, ST_BWD_WAIT | 0x1a))) break;
             mbar_arrive_expect_tx(&bars->v_full[sv], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv], h * 64, krow, w.bh);
+              if (RA_CHECK_BOX(p.chk, SITE_DQ_TMA_V, h * 64, krow, w.bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv], h * 64, krow,
+                            w.bh);
             ++nv;
           }
         }
@@ -751,7 +766,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       {
         uint32_t v[32];
         const uint4* s4 = reinterpret_cast<const uint4*>(Q + grow * HD + 64 * grp);
-        const bool inb = w.i * g.c + rq < p.S;
+        const bool inb = w.i * g.c + rq < p.S &&
+                         RA_CHECK_RANGE(p.chk, SITE_DQ_Q, grow * HD + 64 * grp, 64, p.BH * p.S * HD);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 x = inb ? __ldg(s4 + k) : make_uint4(0u, 0u, 0u, 0u);
@@ -766,9 +782,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       tc_fence_before();
       mbar_arrive(&bars->qo_full);
       const int64_t vr = vec_row(g, w.bh, w.i, w.r0 / BT) + row;
-      const float nl = p.nlse2[vr];        // -inf past the block end: P = 0
+      const bool vr_ok = RA_CHECK_RANGE(p.chk, SITE_DQ_VEC, vr, 1, p.vec_rows);
+      const float nl = vr_ok ? p.nlse2[vr] : -INFINITY;   // -inf past the block end: P = 0
       const float2 nl2 = make_float2(nl, nl);
-      const float2 nd2 = make_float2(p.ndvec[vr], p.ndvec[vr]);
+      const float ndv = vr_ok ? p.ndvec[vr] : 0.f;
+      const float2 nd2 = make_float2(ndv, ndv);
       for (int s = 0; s < g.N && ok; ++s) {
         const int j = ring_block(w.i, s, g.N);
         if (!block_visited(g, w.i, j)) continue;
@@ -831,10 +849,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       if (!(ok = mbar_wait(&bars->dq_full, dq_ph, wc, ST_BWD_WAIT | 0x19))) break;
       dq_ph ^= 1;
       tc_fence_after();
+      const bool st_ok =
+          rq < g.c && RA_CHECK_RANGE(p.chk, SITE_DQ_OUT, grow * HD + grp * 64, 64, p.BH * p.S * HD);
       if (p.accumulate)
-        add_row_f32(T_DQ + lane_off + grp * 64, p.dQf + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
+        add_row_f32(T_DQ + lane_off + grp * 64, p.dQf + grow * HD + grp * 64, p.inv_sqrt_d, st_ok, 64);
       else
-        store_row_bf16(T_DQ + lane_off + grp * 64, p.dQ + grow * HD + grp * 64, p.inv_sqrt_d, rq < g.c, 64);
+        store_row_bf16(T_DQ + lane_off + grp * 64, p.dQ + grow * HD + grp * 64, p.inv_sqrt_d, st_ok, 64);
       tc_fence_before();
       mbar_arrive(&bars->dq_empty);
     }
@@ -854,7 +874,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
 // main kernels add them with packed f32x2 FMAs and adds.
 __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LSE,
-                                                   float* nlse2, float* ndvec, RingGeom g, int S, int64_t rows) {
+                                                   float* nlse2, float* ndvec, RingGeom g, int S, int64_t rows,
+                                                   int64_t n_rows, CheckRec* chk) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows) return;
@@ -866,7 +887,9 @@ __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restri
   const int64_t bh = t2 / g.N;
   const int lr = qt * BT + r;
   float dv = 0.f, l2 = INFINITY;   // D_vec and LSE*log2(e)
-  if (lr < g.c) {
+  if (lr < g.c && RA_CHECK_RANGE(chk, SITE_PREP_IN, (bh * S + static_cast<int64_t>(i) * g.c + lr) * HD + lane * 4, 4,
+                                 n_rows * HD) &&
+      RA_CHECK_RANGE(chk, SITE_PREP_LSE, bh * S + static_cast<int64_t>(i) * g.c + lr, 1, n_rows)) {
     const int64_t row = bh * S + static_cast<int64_t>(i) * g.c + lr;
     const uint2 a = *reinterpret_cast<const uint2*>(O + row * HD + lane * 4);
     const uint2 b = *reinterpret_cast<const uint2*>(dO + row * HD + lane * 4);
@@ -886,7 +909,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __nv_bfloat16* __restri
     const float l = LSE[row];
     l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
   }
-  if (lane == 0) {
+  if (lane == 0 && RA_CHECK_RANGE(chk, SITE_PREP_OUT, w, 1, rows)) {
     nlse2[w] = -l2;
     ndvec[w] = -dv;
   }
@@ -920,27 +943,25 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.dKf = a.accumulate ? static_cast<float*>(a.dK) : nullptr;
   p.dVf = a.accumulate ? static_cast<float*>(a.dV) : nullptr;
   p.status = a.status;
+  p.BH = a.B * a.H;
+  p.chk = a.chk;
   const CUtensorMap& mq = *static_cast<const CUtensorMap*>(tmap_q);
   const CUtensorMap& mk = *static_cast<const CUtensorMap*>(tmap_k);
   const CUtensorMap& mv = *static_cast<const CUtensorMap*>(tmap_v);
   const CUtensorMap& mdo = *static_cast<const CUtensorMap*>(tmap_do);
 
   const int64_t prow = a.B * a.H * a.N * p.g.n_mb * BT;   // padded query rows
+  p.vec_rows = prow;
   if (a.ev) cudaEventRecord(a.ev[0], a.stream);
   prep_kernel<<<static_cast<unsigned>((prow * 32 + 255) / 256), 256, 0, a.stream>>>(
       static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.LSE, a.nlse2, a.ndvec, p.g,
-      p.S, prow);
+      p.S, prow, a.B * a.H * a.S, a.chk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  static bool attr_done = false;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(kv::dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kv::SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(q::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, q::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  e = raise_smem_limit(reinterpret_cast<const void*>(kv::dkv_kernel), kv::SMEM_BYTES);
+  if (e == cudaSuccess) e = raise_smem_limit(reinterpret_cast<const void*>(q::dq_kernel), q::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   const int64_t units = a.B * a.H * a.N * p.g.n_kt;   // KV tiles = query tiles
   p.num_units = units;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);

@@ -1,8 +1,9 @@
 // bwd_noalloc.cu -- ra_bwd_noalloc: the backward pass for callers that cannot
 // allocate device memory.
 //
-// ra_bwd needs a float32 workspace (the dQ accumulator plus two per-row
-// vectors) that the caller allocates.  Some callers cannot do that: a plugin
+// ra_bwd needs a workspace that the caller allocates: two float32 vectors
+// per padded query row (-LSE*log2(e) and -D_vec, rows padded to 128-row
+// tiles per ring block).  Some callers cannot do that: a plugin
 // running inside a host framework that owns every byte of device memory
 // through its own pool and forbids side allocations, or a latency-critical
 // path that must not call cudaMalloc (which can synchronise the whole

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "checks.cuh"
+
 namespace ra {
 
 // Geometry of one call.  The sequence of S rows is cut into N blocks of
@@ -129,8 +131,12 @@ enum : unsigned int {
   ST_BWD_WAIT = 0x200,
   ST_DEC_WAIT = 0x300,
   ST_FFN_WAIT = 0x400,
-  ST_PROBE_WAIT = 0x500,
 };
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute is per device, so a process driving
+// several GPUs sets it on each).  Thread-safe; defined in host.cu.
+cudaError_t raise_smem_limit(const void* func, int bytes);
 
 // ----------------------------------------------------------- launchers
 // All return cudaError_t of the launch; arguments are validated by the caller.
@@ -149,12 +155,15 @@ struct FwdArgs {
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t* ev;             // null, or 2 events recorded before/after the kernel
+  CheckRec* chk;               // per-device check record (used by the checked build only)
 };
 cudaError_t launch_fwd_f32(const FwdArgs& a);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v);
+// Operand types of the merge: state O_a / partial O_b.
+enum : int { MERGE_F32 = 0, MERGE_BF16 = 1, MERGE_F32_BF16 = 2 };
 cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
-                         int64_t D, int bf16, cudaStream_t stream, int num_sms);
+                         int64_t D, int kind, cudaStream_t stream, int num_sms, CheckRec* chk);
 cudaError_t launch_fill(float* x, int64_t n, float value, cudaStream_t stream, int num_sms);
 
 struct BwdArgs {
@@ -177,6 +186,7 @@ struct BwdArgs {
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t* ev;   // null, or 4 events: before prep, dK/dV and dQ kernels, and after
+  CheckRec* chk;
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v, const void* tmap_do);
@@ -221,6 +231,7 @@ struct DecodeArgs {
   cudaStream_t stream;
   int num_sms;
   cudaEvent_t* ev;   // null, or 3 events: before the split kernel, between, after the combine
+  CheckRec* chk;
 };
 cudaError_t launch_decode_bf16(const DecodeArgs& a);
 
@@ -238,11 +249,9 @@ struct FfnGemmArgs {
   int num_sms;
   int overlap_previous;   // 1: may start while the previous launch (of the same call) drains
   int* tile_counter;      // device int, zero before the launch (dynamic tile scheduler)
+  CheckRec* chk;
 };
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void* tmap_b0, const void* tmap_b1);
 
-// Tensor-core issue-rate probe (synchronous; measurement aid).
-cudaError_t launch_probe_mma(int ts, int n, int iters, int switch_every, int variant, int num_sms,
-                             unsigned int* status, double* clk_per_mma);
 
 }  // namespace ra

@@ -63,6 +63,8 @@ struct Params {
   int N;
   float scale_log2;         // log2(e) / sqrt(HD)
   unsigned int* status;
+  int64_t BH;
+  CheckRec* chk;
 };
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -117,8 +119,9 @@ __global__ void __launch_bounds__(THREADS, 2) split_kernel(const Params p) {
           const uint32_t bytes = static_cast<uint32_t>(min64(R, hi - r0)) * ROW_BYTES;
           const int st = ns % NST;
           if (!(ok = mbar_wait(&bars->empty[st], ((ns / NST) & 1) ^ 1, wc, ST_DEC_WAIT | 1))) break;
-          mbar_arrive_expect_tx(&bars->full[st], 2 * bytes);
           const int64_t g = (bh * p.S + r0) * HD;
+          if (!(ok = RA_CHECK_RANGE(p.chk, SITE_DEC_KV, g, bytes / 2, p.BH * p.S * HD))) break;
+          mbar_arrive_expect_tx(&bars->full[st], 2 * bytes);
           bulk_load(smem + st * STAGE_BYTES, p.K + g, bytes, &bars->full[st]);
           bulk_load(smem + st * STAGE_BYTES + HALF_STAGE, p.V + g, bytes, &bars->full[st]);
         }
@@ -140,8 +143,9 @@ __global__ void __launch_bounds__(THREADS, 2) split_kernel(const Params p) {
   for (int64_t w = blockIdx.x; w < p.items; w += gridDim.x) {
     int64_t bh, lo, hi;
     item_rows(p, w, bh, lo, hi);
-    float qv[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p.q + bh * HD + dg * 8), qv);
+    float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (RA_CHECK_RANGE(p.chk, SITE_DEC_Q, bh * HD + dg * 8, 8, p.BH * HD))
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(p.q + bh * HD + dg * 8), qv);
 #pragma unroll
     for (int i = 0; i < 8; ++i) qv[i] *= p.scale_log2;
     float m = -INFINITY, l = 0.f, o[8];
@@ -216,8 +220,10 @@ __global__ void __launch_bounds__(THREADS, 2) split_kernel(const Params p) {
           acc = fmaf(state[r * STATE_FLOATS + tid], wr, acc);
         }
       }
-      p.part_o[w * HD + tid] = M == -INFINITY ? 0.f : acc / L;
-      if (tid == 0) p.part_lse[w] = M == -INFINITY ? -INFINITY : (M + hw_log2(L)) * LN2;
+      if (RA_CHECK_RANGE(p.chk, SITE_DEC_PART, w * HD + tid, 1, p.items * HD)) {
+        p.part_o[w * HD + tid] = M == -INFINITY ? 0.f : acc / L;
+        if (tid == 0) p.part_lse[w] = M == -INFINITY ? -INFINITY : (M + hw_log2(L)) * LN2;
+      }
     }
     consumers_sync();
   }
@@ -226,10 +232,12 @@ __global__ void __launch_bounds__(THREADS, 2) split_kernel(const Params p) {
 // One CTA (HD threads) per (b, h): merge the head's n partials.
 __global__ void __launch_bounds__(HD) combine_kernel(const float* __restrict__ part_o,
                                                      const float* __restrict__ part_lse, int64_t n,
-                                                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE) {
+                                                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
+                                                     CheckRec* chk) {
   __shared__ float red[HD / 32];
   const int64_t bh = blockIdx.x;
   const int d = threadIdx.x;
+  if (!RA_CHECK_RANGE(chk, SITE_DEC_PART, bh * n * HD, n * HD, static_cast<int64_t>(gridDim.x) * n * HD)) return;
   const float* lse = part_lse + bh * n;
   const float* po = part_o + bh * n * HD;
   float M = -INFINITY;
@@ -251,6 +259,7 @@ __global__ void __launch_bounds__(HD) combine_kernel(const float* __restrict__ p
       acc = fmaf(wi, po[i * HD + d], acc);
     }
   }
+  if (!RA_CHECK_RANGE(chk, SITE_DEC_OUT, bh * HD + d, 1, static_cast<int64_t>(gridDim.x) * HD)) return;
   O[bh * HD + d] = __float2bfloat16_rn(M == -INFINITY ? 0.f : acc / L);
   if (d == 0) LSE[bh] = M == -INFINITY ? -INFINITY : M + logf(L);
 }
@@ -259,13 +268,8 @@ __global__ void __launch_bounds__(HD) combine_kernel(const float* __restrict__ p
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a) {
   static_assert(dec::SMEM_BYTES <= 232448 / 2, "two CTAs per SM");
-  static bool attr_done = false;  // benign race: idempotent attribute set
-  cudaError_t e;
-  if (!attr_done) {
-    e = cudaFuncSetAttribute(dec::split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(dec::split_kernel), dec::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   dec::Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.K = static_cast<const __nv_bfloat16*>(a.K);
@@ -280,6 +284,8 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a) {
   p.N = static_cast<int>(a.N);
   p.scale_log2 = dec::LOG2E / sqrtf(static_cast<float>(dec::HD));
   p.status = a.status;
+  p.BH = a.B * a.H;
+  p.chk = a.chk;
   const int64_t slots = 2 * static_cast<int64_t>(a.num_sms);
   const int grid = static_cast<int>(p.items < slots ? p.items : slots);
   if (a.ev) cudaEventRecord(a.ev[0], a.stream);
@@ -288,7 +294,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a) {
   if (e != cudaSuccess) return e;
   if (a.ev) cudaEventRecord(a.ev[1], a.stream);
   dec::combine_kernel<<<static_cast<unsigned>(a.B * a.H), dec::HD, 0, a.stream>>>(
-      a.part_o, a.part_lse, a.plan.items / (a.B * a.H), static_cast<__nv_bfloat16*>(a.O), a.LSE);
+      a.part_o, a.part_lse, a.plan.items / (a.B * a.H), static_cast<__nv_bfloat16*>(a.O), a.LSE, a.chk);
   e = cudaGetLastError();
   if (a.ev) cudaEventRecord(a.ev[2], a.stream);
   return e;

@@ -72,6 +72,8 @@ struct Params {
   int64_t ldo;
   int* tile_counter;     // zero before the launch
   unsigned int* status;
+  int K, b_rows;         // A and B maps: K columns; B map rows (W1/W3: f, W2: h)
+  CheckRec* chk;
 };
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc(saddr, 16, 1024, SWZ_128B); }
@@ -149,9 +151,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           if (!(ok = mbar_wait(&bars->empty[st], ((it / STAGES) & 1) ^ 1, wc, ST_FFN_WAIT | 1))) break;
           mbar_arrive_expect_tx(&bars->full[st], STAGE_BYTES);
           uint8_t* s = smem + st * STAGE_BYTES;
-          tma_load_3d(s, &tmA, &bars->full[st], kc * BK, m * BM, 0);
-          tma_load_3d(s + A_BYTES, &tmB0, &bars->full[st], kc * BK, n * p.b_row_step, 0);
-          tma_load_3d(s + A_BYTES + B_BYTES / 2, &tmB1, &bars->full[st], kc * BK, n * p.b_row_step + p.b1_row_off, 0);
+          if (RA_CHECK_BOX(p.chk, SITE_FFN_TMA, kc * BK, m * BM, 0, p.K, p.M, 1, 8))
+            tma_load_3d(s, &tmA, &bars->full[st], kc * BK, m * BM, 0);
+          if (RA_CHECK_BOX(p.chk, SITE_FFN_TMA, kc * BK, n * p.b_row_step, 0, p.K, p.b_rows, 1, 8))
+            tma_load_3d(s + A_BYTES, &tmB0, &bars->full[st], kc * BK, n * p.b_row_step, 0);
+          if (RA_CHECK_BOX(p.chk, SITE_FFN_TMA, kc * BK, n * p.b_row_step + p.b1_row_off, 0, p.K, p.b_rows, 1, 8))
+            tma_load_3d(s + A_BYTES + B_BYTES / 2, &tmB1, &bars->full[st], kc * BK, n * p.b_row_step + p.b1_row_off,
+                        0);
         }
       }
       for (uint32_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
@@ -207,7 +213,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       if (!mbar_wait(&bars->acc_full[buf], (lt >> 1) & 1, wc, ST_FFN_WAIT | 4)) break;
       tc_fence_after();
       const int row = m * BM + quad * 32 + lane;
-      const bool ok = row < p.M;
+      [[maybe_unused]] const int64_t out_cols = p.gated ? 128 : BN;
+      const bool ok = row < p.M && RA_CHECK_RANGE(p.chk, SITE_FFN_OUT, static_cast<int64_t>(row) * p.ldo + n * out_cols,
+                                                  out_cols, static_cast<int64_t>(p.M) * p.ldo);
       const uint32_t acc = tmem + buf * BN + lane_off;
       if (p.gated) {
         __nv_bfloat16* dst = p.out + static_cast<int64_t>(row) * p.ldo + static_cast<int64_t>(n) * 128;
@@ -257,12 +265,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 }  // namespace ffn
 
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void* tmap_b0, const void* tmap_b1) {
-  static bool attr_done = false;  // benign race: idempotent attribute set
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(ffn::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ffn::SMEM_BYTES);
+  {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(ffn::gemm_kernel), ffn::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   ffn::Params p;
   p.m_tiles = static_cast<int>((a.M + ffn::BM - 1) / ffn::BM);
@@ -276,6 +281,9 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, const void* tmap_a, const void
   p.ldo = a.ldo;
   p.tile_counter = a.tile_counter;
   p.status = a.status;
+  p.K = static_cast<int>(a.K);
+  p.b_rows = static_cast<int>(a.N);
+  p.chk = a.chk;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const int grid = static_cast<int>(tiles < a.num_sms ? tiles : a.num_sms);
   cudaLaunchConfig_t cfg = {};

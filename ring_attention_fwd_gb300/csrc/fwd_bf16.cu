@@ -77,6 +77,8 @@ struct Params {
   unsigned int* status;
   unsigned long long* timing;      // [N*N] ns accumulators or null
   int withhold_first_q;            // test aid: never load the first unit's Q (waits then time out)
+  int64_t BH;                      // heads (B*H): extent of the tensors' third TMA dimension
+  CheckRec* chk;
 };
 
 // K-major operand tile (rows x 128 cols bf16, two 128B-swizzled 64-col boxes):
@@ -157,8 +159,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const int qrow = w.i * g.c + w.r0;
           for (int q = 0; q < 2; ++q)
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_Q + q * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full, h * 64,
-                          qrow + q * BM, w.bh);
+              if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_Q, h * 64, qrow + q * BM, w.bh, HD, p.S + BM, p.BH, 8))
+                tma_load_3d(smem + OFF_Q + q * TILE_BYTES + h * BOX_BYTES, &tmQ, &bars->q_full, h * 64,
+                            qrow + q * BM, w.bh);
         }
         ++nq;
         for (int s = 0; s < g.N && ok; ++s) {
@@ -171,14 +174,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!(ok = mbar_wait(&bars->k_empty[sk], ((kv_it / KSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 2))) break;
             mbar_arrive_expect_tx(&bars->k_full[sk], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk],
-                          h * 64, krow, w.bh);
+              if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_K, h * 64, krow, w.bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_K + sk * TILE_BYTES + h * BOX_BYTES, &tmK, &bars->k_full[sk],
+                            h * 64, krow, w.bh);
             ++nk;
             if (!(ok = mbar_wait(&bars->v_empty[sv], ((kv_it / VSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 11))) break;
             mbar_arrive_expect_tx(&bars->v_full[sv], TILE_BYTES);
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv],
-                          h * 64, krow, w.bh);
+              if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_V, h * 64, krow, w.bh, HD, p.S, p.BH, 8))
+                tma_load_3d(smem + OFF_V + sv * TILE_BYTES + h * BOX_BYTES, &tmV, &bars->v_full[sv],
+                            h * 64, krow, w.bh);
             ++kv_it;
           }
         }
@@ -339,6 +344,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             m_use = mt;
           }
           const bool rescale_o = (t > 0) && __any_sync(0xffffffffu, grow);
+#if RA_CHECKS
+          if (rescale_o && grow) RA_COUNT(p.chk, EV_FWD_RESCALE_ROWS, 1);
+          if (rescale_o && lane == 0) RA_COUNT(p.chk, EV_FWD_RESCALE_WARPS, 1);
+#endif
           const float mref = (m_use == -INFINITY) ? 0.f : m_use;
           const float2 nm2 = make_float2(-mref, -mref);
           // Exponent arguments and the row sum two lanes at a time (packed
@@ -385,10 +394,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       tc_fence_after();
       if (p.timing && warp == 2 && lane == 0 && s_prev >= 0)
         atomicAdd(&p.timing[w.i * g.N + s_prev], globaltimer_ns() - t_step0);
-      const bool valid = rq < g.c;
+      bool valid = rq < g.c;
       const int64_t grow_idx = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.O + grow_idx * HD;
+      if (valid && !RA_CHECK_RANGE(p.chk, SITE_FWD_O, grow_idx * HD, HD, p.BH * p.S * HD)) valid = false;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t ov[32];
@@ -405,7 +415,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (valid) p.LSE[grow_idx] = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
+      if (valid && RA_CHECK_RANGE(p.chk, SITE_FWD_LSE, grow_idx, 1, p.BH * p.S)) p.LSE[grow_idx] = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
       tc_fence_before();
       mbar_arrive(&bars->o_empty[q]);
     }
@@ -441,11 +451,11 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   p.status = a.status;
   p.timing = a.timing;
   p.withhold_first_q = a.withhold_first_q;
-  static bool attr_done = false;  // benign race: idempotent attribute set
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  p.BH = a.B * a.H;
+  p.chk = a.chk;
+  {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(fwd_kernel), SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t grid64 = p.num_units < a.num_sms ? p.num_units : a.num_sms;
   const int grid = static_cast<int>(grid64 > 0 ? grid64 : 1);

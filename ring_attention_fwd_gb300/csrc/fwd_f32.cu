@@ -34,6 +34,8 @@ struct Params {
   const float* V;
   float* O;
   float* LSE;
+  int64_t n_rows;   // B*H*S: extent of Q, K, V, O (rows of D) and LSE
+  CheckRec* chk;
 };
 
 __global__ void __launch_bounds__(THREADS) fwd_f32_kernel(const Params p) {
@@ -58,7 +60,8 @@ __global__ void __launch_bounds__(THREADS) fwd_f32_kernel(const Params p) {
     for (int e = tid; e < BM * D; e += THREADS) {
       const int rr = e / D, d = e % D;
       const int lr = w.r0 + rr;
-      sQ[e] = (lr < g.c) ? p.Q[(head0 + static_cast<int64_t>(w.i) * g.c + lr) * D + d] : 0.f;
+      const int64_t qi = (head0 + static_cast<int64_t>(w.i) * g.c + lr) * D + d;
+      sQ[e] = (lr < g.c && RA_CHECK_RANGE(p.chk, SITE_F32_Q, qi, 1, p.n_rows * D)) ? p.Q[qi] : 0.f;
     }
     float m = -INFINITY, l = 0.f;
     float o[DMAX / 4];
@@ -75,8 +78,8 @@ __global__ void __launch_bounds__(THREADS) fwd_f32_kernel(const Params p) {
         for (int e = tid; e < BN * D; e += THREADS) {
           const int rr = e / D, d = e % D;
           const int lk = kt * BN + rr;
-          const bool in = lk < g.c;
           const int64_t gi = (head0 + static_cast<int64_t>(j) * g.c + lk) * D + d;
+          const bool in = lk < g.c && RA_CHECK_RANGE(p.chk, SITE_F32_KV, gi, 1, p.n_rows * D);
           sK[rr * ldk + d] = in ? p.K[gi] : 0.f;
           sV[rr * D + d] = in ? p.V[gi] : 0.f;
         }
@@ -123,8 +126,10 @@ __global__ void __launch_bounds__(THREADS) fwd_f32_kernel(const Params p) {
         }
       }
     }
-    if (rq < g.c) {
-      const int64_t row = head0 + static_cast<int64_t>(w.i) * g.c + rq;
+    const int64_t orow = head0 + static_cast<int64_t>(w.i) * g.c + rq;
+    if (rq < g.c && RA_CHECK_RANGE(p.chk, SITE_F32_O, orow * D, D, p.n_rows * D) &&
+        RA_CHECK_RANGE(p.chk, SITE_F32_LSE, orow, 1, p.n_rows)) {
+      const int64_t row = orow;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int cc = 0; cc < DMAX / 4; ++cc)
@@ -152,19 +157,19 @@ cudaError_t launch_fwd_f32(const FwdArgs& a) {
   p.D = static_cast<int>(a.D);
   p.num_units = a.B * a.H * a.N * p.g.n_mb;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
+  p.n_rows = a.B * a.H * a.S;
+  p.chk = a.chk;
   p.Q = static_cast<const float*>(a.Q);
   p.K = static_cast<const float*>(a.K);
   p.V = static_cast<const float*>(a.V);
   p.O = static_cast<float*>(a.O);
   p.LSE = a.LSE;
   const size_t smem = sizeof(float) * (BM * a.D + BN * (a.D + 1) + BN * a.D + BM * (BN + 1));
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(float) * (BM * DMAX + BN * (DMAX + 1) +
-                                                                           BN * DMAX + BM * (BN + 1))));
+  {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(fwd_f32_kernel),
+                                     static_cast<int>(sizeof(float) * (BM * DMAX + BN * (DMAX + 1) +
+                                                                       BN * DMAX + BM * (BN + 1))));
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const int64_t cap = static_cast<int64_t>(a.num_sms) * 8;
   const int grid = static_cast<int>(p.num_units < cap ? p.num_units : cap);

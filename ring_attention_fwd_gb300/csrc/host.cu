@@ -10,9 +10,12 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <deque>
 #include <map>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <string>
 #include <vector>
 
@@ -38,12 +41,14 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ---------------------------------------------------------------- device state
 __device__ unsigned int g_device_status;  // first bounded-wait time-out code, 0 if none
+__device__ ra::CheckRec g_check_rec;      // bounds checks and event counts (checked build)
 
 constexpr int kMaxDevices = 64;
 struct DevState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;  // device address of g_device_status
+  ra::CheckRec* chk = nullptr;     // device address of g_check_rec
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -67,6 +72,9 @@ int device_state(DevState** out) {
     e = cudaGetSymbolAddress(&p, g_device_status);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
     d.status = static_cast<unsigned int*>(p);
+    e = cudaGetSymbolAddress(&p, g_check_rec);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(check record)");
+    d.chk = static_cast<ra::CheckRec*>(p);
     d.ready = true;
   }
   *out = &d;
@@ -207,6 +215,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
   a.ev = kt_begin(RA_CALL_FWD, 1);
+  a.chk = d->chk;
   cudaError_t e;
   if (dtype == RA_BF16) {
     CUtensorMap mq, mk, mv;
@@ -226,12 +235,44 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
 namespace ra {
 // Lets other translation units of the library report through ra_last_error().
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+cudaError_t raise_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;   // (device, kernel) pairs already raised
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({dev, func})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({dev, func});
+  return e;
+}
 }  // namespace ra
 
 extern "C" {
 
 const char* ra_last_error(void) { return g_last_error.c_str(); }
-const char* ra_version(void) { return "ringattn 0.1 sm_103a"; }
+const char* ra_version(void) { return RA_CHECKS ? "ringattn 0.2 sm_103a checked" : "ringattn 0.2 sm_103a"; }
+
+int ra_read_checks(ra_check_report* out, void* stream) {
+  static_assert(sizeof(ra_check_report) == sizeof(ra::CheckRec), "report layout mirrors the device record");
+  if (!out) return fail(RA_ERR_ARG, "ra_read_checks: null pointer");
+  if (!RA_CHECKS) return fail(RA_ERR_UNSUPPORTED, "ra_read_checks: this is not the checked build");
+  DevState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc != RA_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  ra::CheckRec r;
+  e = cudaMemcpyFromSymbol(&r, g_check_rec, sizeof(r));
+  if (e != cudaSuccess) return cuda_fail(e, "read check record");
+  const ra::CheckRec zero = {};
+  e = cudaMemcpyToSymbol(g_check_rec, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear check record");
+  memcpy(out, &r, sizeof(r));
+  return RA_OK;
+}
 
 int ra_set_timing_buffer(uint64_t* dev_buf, size_t n) {
   if (dev_buf != nullptr && n < 1) return fail(RA_ERR_ARG, "timing buffer of size 0");
@@ -344,18 +385,20 @@ int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64
              void* stream) {
   if (rows < 0) return fail(RA_ERR_ARG, "ra_merge: rows < 0");
   if (D < 1 || D > 1024) return fail(RA_ERR_ARG, "ra_merge: D must be in 1..1024 (got %lld)", (long long)D);
-  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_ARG, "bad dtype %d", dtype);
+  if (dtype != RA_F32 && dtype != RA_BF16 && dtype != RA_F32_BF16)
+    return fail(RA_ERR_ARG, "ra_merge: bad dtype %d", dtype);
   if (rows == 0) return RA_OK;
   if (!O_a || !lse_a || !O_b || !lse_b) return fail(RA_ERR_ARG, "ra_merge: null pointer");
-  const uintptr_t oal = dtype == RA_BF16 ? 2 : 4;
-  if (!aligned(O_a, oal) || !aligned(O_b, oal) || !aligned(lse_a, 4) || !aligned(lse_b, 4))
+  const uintptr_t aal = dtype == RA_BF16 ? 2 : 4, bal = dtype == RA_F32 ? 4 : 2;
+  if (!aligned(O_a, aal) || !aligned(O_b, bal) || !aligned(lse_a, 4) || !aligned(lse_b, 4))
     return fail(RA_ERR_ARG, "ra_merge: misaligned pointer");
   if (rows > INT64_MAX / D) return fail(RA_ERR_ARG, "ra_merge: rows*D overflows");
   DevState* d = nullptr;
   int rc = device_state(&d);
   if (rc != RA_OK) return rc;
-  cudaError_t e = ra::launch_merge(O_a, lse_a, O_b, lse_b, rows, D, dtype == RA_BF16,
-                                   static_cast<cudaStream_t>(stream), d->num_sms);
+  const int kind = dtype == RA_BF16 ? ra::MERGE_BF16 : dtype == RA_F32_BF16 ? ra::MERGE_F32_BF16 : ra::MERGE_F32;
+  cudaError_t e = ra::launch_merge(O_a, lse_a, O_b, lse_b, rows, D, kind, static_cast<cudaStream_t>(stream),
+                                   d->num_sms, d->chk);
   if (e != cudaSuccess) return cuda_fail(e, "ra_merge launch");
   return RA_OK;
 }
@@ -431,6 +474,7 @@ int bwd_impl(const char* who, const void* Q, const void* K, const void* V, const
   a.status = d->status;
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
+  a.chk = d->chk;
   CUtensorMap mq, mk, mv, mdo;
   if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
@@ -535,6 +579,7 @@ int ra_decode(const void* q, const void* K, const void* V, int64_t B, int64_t H,
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
   a.ev = kt_begin(RA_CALL_DECODE, 2);
+  a.chk = d->chk;
   cudaError_t e = ra::launch_decode_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "ra_decode launch");
   return RA_OK;
@@ -600,8 +645,8 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
     if ((rc = make_map_bf16(&mh, workspace, 1, rows, f, 128)) != RA_OK) return rc;
     // The first launch keeps full stream order (X may come from the caller's
     // previous kernel); later ones overlap the previous launch's last wave.
-    ra::FfnGemmArgs up{rows, f, h, 1, workspace, f, d->status, st, d->num_sms, b > 0 ? 1 : 0, counters + 2 * b};
-    ra::FfnGemmArgs down{rows, h, f, 0, yb, h, d->status, st, d->num_sms, 1, counters + 2 * b + 1};
+    ra::FfnGemmArgs up{rows, f, h, 1, workspace, f, d->status, st, d->num_sms, b > 0 ? 1 : 0, counters + 2 * b, d->chk};
+    ra::FfnGemmArgs down{rows, h, f, 0, yb, h, d->status, st, d->num_sms, 1, counters + 2 * b + 1, d->chk};
     if (ev) cudaEventRecord(ev[2 * b], st);
     cudaError_t e = ra::launch_ffn_gemm(up, &mx, &m1, &m3);
     if (e != cudaSuccess) return cuda_fail(e, "ra_ffn launch (up)");
@@ -610,27 +655,6 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
     if (e != cudaSuccess) return cuda_fail(e, "ra_ffn launch (down)");
   }
   if (ev) cudaEventRecord(ev[2 * nblocks], st);
-  return RA_OK;
-}
-
-}  // extern "C"
-
-extern "C" {
-
-int ra_probe_mma(int a_from_tmem, int n, int iters, int switch_every, int variant, double* clk_per_mma) {
-  if (!clk_per_mma) return fail(RA_ERR_ARG, "ra_probe_mma: null pointer");
-  if (a_from_tmem != 0 && a_from_tmem != 1) return fail(RA_ERR_ARG, "ra_probe_mma: a_from_tmem must be 0 or 1");
-  if (n < 16 || n > 256 || n % 16 != 0) return fail(RA_ERR_ARG, "ra_probe_mma: n must be a multiple of 16 in 16..256");
-  if (iters < 1 || iters > 10000000) return fail(RA_ERR_ARG, "ra_probe_mma: iters must be in 1..10^7");
-  if (switch_every < 0 || (switch_every > 0 && n > 128))
-    return fail(RA_ERR_ARG, "ra_probe_mma: switch_every >= 0, and two accumulators need n <= 128");
-  if (variant < 0 || variant > 63) return fail(RA_ERR_ARG, "ra_probe_mma: variant must be in 0..63");
-  DevState* d = nullptr;
-  int rc = device_state(&d);
-  if (rc != RA_OK) return rc;
-  cudaError_t e =
-      ra::launch_probe_mma(a_from_tmem, n, iters, switch_every, variant, d->num_sms, d->status, clk_per_mma);
-  if (e != cudaSuccess) return cuda_fail(e, "ra_probe_mma");
   return RA_OK;
 }
 

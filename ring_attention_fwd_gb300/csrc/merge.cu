@@ -6,7 +6,10 @@
 // normalised outputs are re-weighted by each part's share of the total mass.
 //
 // HBM-bound elementwise kernel: each block owns whole rows, so every thread
-// reads lse_a of its row before any thread of the block overwrites it.
+// reads lse_a of its row before any thread of the block overwrites it.  The
+// state (O_a) and the partial (O_b) are both float32, both bf16, or a float32
+// state folding a bf16 partial (a ring host keeping its running output in
+// float32 across rounds while each round's partial arrives in bf16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,20 +30,26 @@ template <>
 struct Vec<__nv_bfloat16, 8> {
   using type = uint4;
 };
+template <>
+struct Vec<__nv_bfloat16, 4> {
+  using type = uint2;
+};
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float v, float& x) { x = v; }
 __device__ __forceinline__ void from_f(float v, __nv_bfloat16& x) { x = __float2bfloat16_rn(v); }
 
-template <typename T, int VEC>
-__global__ void __launch_bounds__(1024) merge_kernel(T* __restrict__ Oa, float* la, const T* __restrict__ Ob,
-                                                     const float* lb, int64_t rows, int D, int cpr, int rpb) {
+template <typename T, typename TB, int VEC>
+__global__ void __launch_bounds__(1024) merge_kernel(T* __restrict__ Oa, float* la, const TB* __restrict__ Ob,
+                                                     const float* lb, int64_t rows, int D, int cpr, int rpb,
+                                                     CheckRec* chk) {
   const int tid = threadIdx.x;
   const int rsub = tid / cpr;
   const int ch = tid % cpr;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * rpb + rsub;
-  const bool active = rsub < rpb && row < rows;
+  const bool active = rsub < rpb && row < rows && RA_CHECK_RANGE(chk, SITE_MERGE_LSE, row, 1, rows) &&
+                     RA_CHECK_RANGE(chk, SITE_MERGE_O, row * D + static_cast<int64_t>(ch) * VEC, VEC, rows * D);
   float A = -INFINITY, Bv = -INFINITY;
   if (active) {
     A = la[row];
@@ -65,10 +74,11 @@ __global__ void __launch_bounds__(1024) merge_kernel(T* __restrict__ Oa, float* 
     Oa[base] = out;
   } else {
     using V = typename Vec<T, VEC>::type;
+    using VB = typename Vec<TB, VEC>::type;
     V va = *reinterpret_cast<const V*>(Oa + base);
-    V vb = *reinterpret_cast<const V*>(Ob + base);
+    VB vb = *reinterpret_cast<const VB*>(Ob + base);
     T* ea = reinterpret_cast<T*>(&va);
-    const T* eb = reinterpret_cast<const T*>(&vb);
+    const TB* eb = reinterpret_cast<const TB*>(&vb);
 #pragma unroll
     for (int k = 0; k < VEC; ++k) from_f(wa * to_f(ea[k]) + wb * to_f(eb[k]), ea[k]);
     *reinterpret_cast<V*>(Oa + base) = va;
@@ -76,17 +86,17 @@ __global__ void __launch_bounds__(1024) merge_kernel(T* __restrict__ Oa, float* 
   if (ch == 0) la[row] = lse;
 }
 
-template <typename T, int VEC>
+template <typename T, typename TB, int VEC>
 cudaError_t run(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows, int64_t D,
-                cudaStream_t stream) {
+                cudaStream_t stream, CheckRec* chk) {
   const int cpr = static_cast<int>(D / VEC);
   int rpb = 256 / cpr;
   if (rpb < 1) rpb = 1;
   const int threads = rpb * cpr;
   const int64_t blocks = (rows + rpb - 1) / rpb;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  merge_kernel<T, VEC><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<T*>(O_a), lse_a, static_cast<const T*>(O_b), lse_b, rows, static_cast<int>(D), cpr, rpb);
+  merge_kernel<T, TB, VEC><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<T*>(O_a), lse_a, static_cast<const TB*>(O_b), lse_b, rows, static_cast<int>(D), cpr, rpb, chk);
   return cudaGetLastError();
 }
 
@@ -107,15 +117,21 @@ cudaError_t launch_fill(float* x, int64_t n, float value, cudaStream_t stream, i
 }
 
 cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
-                         int64_t D, int bf16, cudaStream_t stream, int /*num_sms*/) {
+                         int64_t D, int kind, cudaStream_t stream, int /*num_sms*/, CheckRec* chk) {
   if (rows == 0) return cudaSuccess;
-  const uintptr_t al = reinterpret_cast<uintptr_t>(O_a) | reinterpret_cast<uintptr_t>(O_b);
-  if (bf16) {
-    if (D % 8 == 0 && (al & 15) == 0) return mrg::run<__nv_bfloat16, 8>(O_a, lse_a, O_b, lse_b, rows, D, stream);
-    return mrg::run<__nv_bfloat16, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+  using bf = __nv_bfloat16;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(O_a), b = reinterpret_cast<uintptr_t>(O_b);
+  if (kind == MERGE_BF16) {
+    if (D % 8 == 0 && ((a | b) & 15) == 0) return mrg::run<bf, bf, 8>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
+    return mrg::run<bf, bf, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
   }
-  if (D % 4 == 0 && (al & 15) == 0) return mrg::run<float, 4>(O_a, lse_a, O_b, lse_b, rows, D, stream);
-  return mrg::run<float, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream);
+  if (kind == MERGE_F32_BF16) {
+    if (D % 4 == 0 && (a & 15) == 0 && (b & 7) == 0)
+      return mrg::run<float, bf, 4>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
+    return mrg::run<float, bf, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
+  }
+  if (D % 4 == 0 && ((a | b) & 15) == 0) return mrg::run<float, float, 4>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
+  return mrg::run<float, float, 1>(O_a, lse_a, O_b, lse_b, rows, D, stream, chk);
 }
 
 }  // namespace ra

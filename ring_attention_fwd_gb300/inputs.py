@@ -46,6 +46,56 @@ def make_inputs(B: int, H: int, S: int, D: int, seed: int, *, dtype: str = "bf16
     return out
 
 
+# Peaked inputs: the structure below makes the running row maximum of the
+# online softmax jump by a known amount, so that the O correction runs.
+PEAK_A = 16.0      # query coordinate
+PEAK_B = 8.0       # key coordinate per ring step (score step A*B/sqrt(128) = 11.3)
+PEAK_PLANT = 40.0  # planted key coordinate (score A*40/sqrt(128) = 56.6)
+
+
+def make_peaked_inputs(B: int, H: int, S: int, N: int, seed: int, mode: str = "ring") -> dict:
+    """bf16 {'q','k','v','do'} [B, H, S, 128] whose scores grow along the ring.
+
+    ``make_inputs`` (seeded, N(0,1)) first; then some coordinates of q and k
+    are overwritten with fixed values (all exact in bf16), the rest stay
+    random.  Storage block i holds rows [i*c, (i+1)*c), c = S/N.
+      * ``ring`` (N <= 64): coordinate x < N of a query row in block i is
+        PEAK_A if x == i, else 0; of a key row in block j it is
+        PEAK_B * ((x - j) mod N).  The score of a block-i query and a block-j
+        key is PEAK_A*PEAK_B*((i - j) mod N)/sqrt(128) plus the random part:
+        it grows by 11.3 at every step of the ring order j = i, i-1, ...
+      * ``tiles``: coordinate 0 of every query is PEAK_A and of a key at row
+        r of its block PEAK_B * (r // 128): scores grow by 11.3 from one
+        128-key tile to the next, inside every block.
+      * ``planted``: coordinate 0 of every query is PEAK_A, of every key 0,
+        except storage row 0 (block 0's first token, which every query sees,
+        and which a contiguous causal sweep meets last) with PEAK_PLANT: that
+        key's score exceeds every other by about 50.
+    v and dO are left as drawn."""
+    if S % N:
+        raise ValueError("S must be a multiple of N")
+    t = make_inputs(B, H, S, 128, seed, with_grad=True)
+    q, k = t["q"], t["k"]
+    c = S // N
+    if mode == "ring":
+        if N > 64:
+            raise ValueError("ring mode needs N <= 64")
+        blk = torch.arange(S) // c                     # storage block of each row
+        x = torch.arange(N)
+        q[..., :N] = torch.where(x[None, :] == blk[:, None], PEAK_A, 0.0).to(q.dtype)
+        k[..., :N] = (PEAK_B * ((x[None, :] - blk[:, None]) % N)).to(k.dtype)
+    elif mode == "tiles":
+        q[..., 0] = PEAK_A
+        k[..., 0] = (PEAK_B * ((torch.arange(S) % c) // 128)).to(k.dtype)
+    elif mode == "planted":
+        q[..., 0] = PEAK_A
+        k[..., 0] = 0.0
+        k[..., 0, 0] = PEAK_PLANT
+    else:
+        raise ValueError(f"unknown mode {mode!r}")
+    return t
+
+
 def as_float64(t: torch.Tensor):
     """Upcast a CPU tensor (bf16 or f32) to a float64 NumPy array, exactly."""
     return t.to(torch.float64).numpy()

@@ -46,7 +46,11 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
     block j; merge(o, lse, o_j, lse_j) folds a partial into (o, lse) in place.
     timeout_s: give up (RuntimeError) if a round's exchange has not completed
     within this many seconds, instead of waiting for a peer that is gone.
-    Returns (o, lse) of this rank's query rows.
+    The running state starts empty (O = 0, lse = -inf) and stays in float32
+    (float64 if q is float64) across the rounds; each round's partial, bf16
+    from the library's step, is folded into it, so the output is rounded once
+    rather than once per round.
+    Returns (o, lse) of this rank's query rows, o in the state's dtype.
     """
     n = dist.get_world_size(group)
     i = dist.get_rank(group)
@@ -57,7 +61,11 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
     send_to, recv_from = (i + 1) % n, (i - 1) % n
     bufs = [(torch.empty_like(k), torch.empty_like(v)) for _ in range(2 if n > 1 else 0)]
     cur_k, cur_v = k, v
-    o = lse = None
+    B, H, c, D = q.shape
+    state = torch.float64 if q.dtype == torch.float64 else torch.float32
+    o = torch.zeros((B, H, c, D), dtype=state, device=q.device)
+    lse = torch.full((B, H, c), float("-inf"), dtype=state if state == torch.float64 else torch.float32,
+                     device=q.device)
     for s, j in enumerate(ring_order(i, n)):
         reqs = []
         if s < n - 1:   # forward the block we hold, receive the next one
@@ -67,10 +75,7 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
             reqs = dist.batch_isend_irecv(ops)
         if not (causal and layout == "contiguous" and j > i):
             oj, lj = step(q, cur_k, cur_v, n, i, j)
-            if o is None:
-                o, lse = oj, lj
-            else:
-                merge(o, lse, oj, lj)
+            merge(o, lse, oj, lj)
         for r in reqs:
             ok = r.wait(datetime.timedelta(seconds=timeout_s)) if timeout_s is not None else r.wait()
             if ok is False:

@@ -101,3 +101,37 @@ def workload_inputs(w: dict, with_grad: bool = False) -> dict:
     leaves Q, K, V unchanged."""
     return make_inputs(w["B"], w["H"], w["S"], w["D"], w["seed"], dtype=w["dtype"], scale=w["scale"],
                        with_grad=w["grad"] or with_grad)
+
+
+def head_arrays(inp: dict, b: int, h: int, names=("q", "k", "v", "do")) -> dict:
+    """float64 NumPy copies of one (b, h) slab of the given inputs (exact)."""
+    return {x: inp[x][b, h].to(torch.float64).numpy() for x in names if x in inp}
+
+
+def keys_in_every_block(S: int, N: int, per_block: int, seed: int) -> np.ndarray:
+    """Storage rows of ``per_block`` keys in each of the N blocks: the block's
+    first row, its last row, and random rows between (sorted, unique)."""
+    c = S // N
+    rng = np.random.default_rng(seed)
+    keys = set()
+    for i in range(N):
+        keys |= {i * c, i * c + c - 1}
+        keys |= set((i * c + rng.integers(0, c, size=max(0, per_block - 2))).tolist())
+    return np.array(sorted(keys), dtype=np.int64)
+
+
+def pooled_fwd_check(inp: dict, o, lse, N: int, causal: bool, layout: str, heads, n_random: int, seed: int):
+    """Sampled rows of every listed head against ``oracle.attention_rows``,
+    computed on all host cores; returns the max errors (O, LSE)."""
+    import oracle_pool as op
+    S = inp["q"].shape[2]
+    eo = el = 0.0
+    for (b, h) in heads:
+        rows = sample_rows(S, N, n_random, seed + 31 * h)
+        paths = op.share(f"fwd{b}_{h}", **head_arrays(inp, b, h, ("q", "k", "v")))
+        ro, rl = op.fwd_rows(paths, rows, N, causal, layout)
+        op.release(paths)
+        idx = torch.from_numpy(rows).to(o.device)
+        eo = max(eo, max_err(o[b, h, idx].float().cpu().numpy(), ro))
+        el = max(el, max_err(lse[b, h, idx].cpu().numpy(), rl))
+    return eo, el

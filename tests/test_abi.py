@@ -14,9 +14,16 @@ HEADER = os.path.join(ROOT, "include", "ringattn.h")
 @pytest.fixture(scope="module")
 def L():
     from ring_attention_fwd_gb300 import binding, build
-    if not os.path.exists(binding._LIB_PATH):
+    if not (os.path.exists(binding._LIB_PATH) and os.path.exists(binding._CHECKED_PATH)):
         build.build()
     return binding.lib()
+
+
+@pytest.fixture(scope="module")
+def LC(L):
+    """The bounds-checked build (loaded beside the default one)."""
+    from ring_attention_fwd_gb300 import binding
+    return binding._load(binding._CHECKED_PATH)
 
 
 def declared_symbols():
@@ -28,8 +35,8 @@ def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
         "ra_decode_workspace_bytes", "ra_decode", "ra_ffn_workspace_bytes", "ra_ffn", "ra_set_timing_buffer",
-        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status", "ra_probe_mma",
-        "ra_last_error", "ra_version"])
+        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status",
+        "ra_read_checks", "ra_last_error", "ra_version"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -39,8 +46,24 @@ def test_library_exports_every_declared_symbol(L):
         assert name in binding.SIGNATURES, name
 
 
+def test_checked_build_exports_every_declared_symbol(LC):
+    for name in declared_symbols():
+        assert hasattr(LC, name), name
+    assert LC.ra_version().decode().endswith("checked")
+
+
 def test_version(L):
     assert L.ra_version().decode().startswith("ringattn")
+    assert not L.ra_version().decode().endswith("checked")
+
+
+def test_read_checks_only_in_checked_build(L, LC):
+    from ring_attention_fwd_gb300 import binding
+    rep = binding.CheckReport()
+    assert L.ra_read_checks(ctypes.addressof(rep), None) == 2
+    assert "not the checked build" in L.ra_last_error().decode()
+    assert LC.ra_read_checks(None, None) == 1 and "null" in LC.ra_last_error().decode()
+    assert ctypes.sizeof(binding.CheckReport) == 88
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
@@ -203,18 +226,6 @@ def test_ffn_workspace_and_bad_arguments(L):
     assert call(X=FAKE + 8) == 1 and "16-byte" in L.ra_last_error().decode()
     assert call(ws=FAKE + 16) == 1 and "256-byte" in L.ra_last_error().decode()
     assert call(ws_bytes=1000) == 1 and "workspace" in L.ra_last_error().decode()
-
-
-def test_probe_rejects_bad_arguments(L):
-    out = ctypes.c_double(0.0)
-    assert L.ra_probe_mma(0, 100, 10, 0, 0, ctypes.byref(out)) == 1 and "multiple of 16" in L.ra_last_error().decode()
-    assert L.ra_probe_mma(0, 512, 10, 0, 0, ctypes.byref(out)) == 1
-    assert L.ra_probe_mma(2, 128, 10, 0, 0, ctypes.byref(out)) == 1
-    assert L.ra_probe_mma(0, 128, 0, 0, 0, ctypes.byref(out)) == 1
-    assert L.ra_probe_mma(0, 256, 10, 8, 0, ctypes.byref(out)) == 1 and "n <= 128" in L.ra_last_error().decode()
-    assert L.ra_probe_mma(0, 128, 10, -1, 0, ctypes.byref(out)) == 1
-    assert L.ra_probe_mma(0, 128, 10, 0, 64, ctypes.byref(out)) == 1
-    assert L.ra_probe_mma(0, 128, 10, 0, 0, None) == 1
 
 
 def test_wait_test_switch_arguments(L):

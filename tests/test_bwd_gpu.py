@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import oracle as orc
-from gpu_helpers import SUM_DK_LIMIT, SUM_DV_LIMIT, TOL, fwd_sampled_check, max_err, sample_rows, workload_inputs
+from gpu_helpers import (SUM_DK_LIMIT, SUM_DV_LIMIT, TOL, fwd_sampled_check, head_arrays, keys_in_every_block,
+                         max_err, sample_rows, workload_inputs)
 from ring_attention_fwd_gb300.inputs import LONG_WORKLOADS, WORKLOADS, as_float64, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -88,18 +89,17 @@ def test_fwd_then_bwd_against_exact_gradient(ra, layout):
     _close(dv.double().cpu().numpy(), rv, "dV")
 
 
-def test_bwd_deterministic_dk_dv_and_workspace_reuse(ra):
-    """dK and dV are written by one CTA each (bit-identical across runs); dQ
-    accumulates with float atomics, so only closeness is required.  A
-    workspace reused without clearing gives the same result."""
+def test_bwd_deterministic_and_workspace_reuse(ra):
+    """dQ, dK and dV are each written once per row by one CTA, with no
+    atomics, so two runs are bit-identical.  A workspace reused without
+    clearing gives the same result."""
     inp = {k: v.cuda() for k, v in make_inputs(1, 2, 1024, 128, seed=5, with_grad=True).items()}
     o, lse = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
     ws = torch.full((ra.bwd_workspace_bytes(1, 2, 1024, 128, 4),), 0x7f, dtype=torch.uint8, device="cuda")
     a = ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped", workspace=ws)
     b = ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped", workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
-    assert float((a[0].float() - b[0].float()).abs().max()) <= 1e-2
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
 def check_sum_identities(dk, dv, do, heads):
@@ -150,17 +150,51 @@ def _sampled_bwd_check(ra, w, dq_heads, kv_head, n_keys, late_only, late_window=
     _close(dv[0, kv_head, kidx].double().cpu().numpy(), rv, "dV rows")
 
 
-def test_fwdbwd_64k_workload_sampled(ra):
-    """The 65536-token striped forward+backward workload at full size: dQ on
-    sampled query rows of two heads, dK/dV on random key rows of one head
-    (every query of that head recomputed by the oracle)."""
-    _sampled_bwd_check(ra, WORKLOADS["fwdbwd_64k"], dq_heads=(0, 31), kv_head=5, n_keys=24, late_only=False)
+def _wide_bwd_check(ra, w, kv_heads, keys_per_block, n_random):
+    """Full-size forward+backward on the GPU, then, with the oracle on all host
+    cores: dQ on sampled rows (every block boundary, random rows) of EVERY
+    head, and dK/dV on keys in EVERY ring block of ``kv_heads`` -- keys of
+    the first blocks are seen by (nearly) every query, so the oracle recomputes
+    the whole head for them.  The sum identities cover every key of every head."""
+    import oracle_pool as op
+    inp = workload_inputs(w, with_grad=True)
+    N, causal, layout = w["N"], w["causal"], w["layout"]
+    B, H, S, D = inp["q"].shape
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
+    o, lse = ra.fwd(dev["q"], dev["k"], dev["v"], N, causal, layout)
+    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, causal, layout)
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t.float()).all())
+    check_sum_identities(dk, dv, dev["do"], range(H))
+    del o, lse, dev
+    for h in range(H):
+        paths = op.share(f"h{h}", **head_arrays(inp, 0, h))
+        rows = sample_rows(S, N, n_random, 7 + h)
+        ref = op.dq_rows(paths, rows, N, causal, layout)
+        _close(dq[0, h, torch.from_numpy(rows).cuda()].double().cpu().numpy(), ref, f"dQ rows head {h}")
+        if h in kv_heads:
+            keys = keys_in_every_block(S, N, keys_per_block, 11 + h)
+            rk, rv = op.kv_rows(paths, keys, N, causal, layout, S)
+            kidx = torch.from_numpy(keys).cuda()
+            _close(dk[0, h, kidx].double().cpu().numpy(), rk, f"dK rows head {h}")
+            _close(dv[0, h, kidx].double().cpu().numpy(), rv, f"dV rows head {h}")
+        op.release(paths)
 
 
-def test_long_128k_workload_backward_sampled(ra):
-    """The benchmark's workload and launch configuration: dQ on sampled rows of
-    two heads, dK/dV on key rows among the last 2048 tokens of one head."""
-    _sampled_bwd_check(ra, WORKLOADS["long_128k"], dq_heads=(0, 20), kv_head=9, n_keys=64, late_only=True)
+def test_fwdbwd_64k_workload_backward_wide(ra):
+    """The 65536-token striped forward+backward workload at full size: dQ rows
+    of all 32 heads; dK/dV on 3 keys of each of the 16 blocks of two heads."""
+    _wide_bwd_check(ra, WORKLOADS["fwdbwd_64k"], kv_heads=(5, 30), keys_per_block=3, n_random=32)
+
+
+def test_long_128k_workload_backward_wide(ra):
+    """The benchmark's workload and launch configuration (131072 tokens, 32
+    blocks, causal contiguous): dQ rows of all 32 heads; dK/dV on 2 keys of
+    each of the 32 blocks of two heads, the early blocks' keys included (the
+    longest ring re-sweeps of the backward)."""
+    _wide_bwd_check(ra, WORKLOADS["long_128k"], kv_heads=(9, 26), keys_per_block=2, n_random=32)
 
 
 def test_million_token_forward_backward_sampled(ra):

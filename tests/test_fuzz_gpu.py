@@ -40,15 +40,21 @@ def test_fuzz_forward_backward(ra, case):
     inp = make_inputs(B, H, S, 128, seed=case["seed"], with_grad=True)
     dev = {k: v.cuda() for k, v in inp.items()}
     o, lse = ra.fwd(dev["q"], dev["k"], dev["v"], N, case["causal"], case["layout"])
-    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], N, case["causal"], case["layout"])
     torch.cuda.synchronize()
     ra.check_device_status()
     q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
     ro, rl = orc.naive_attention(q, k, v, N, case["causal"], case["layout"])
     assert max_err(o.float().cpu().numpy(), ro) <= TOL["bf16"]["o"]
     assert max_err(lse.cpu().numpy(), rl) <= TOL["bf16"]["lse"]
-    # gradients of the definition at the GPU's own saved state (O rounded to bf16, LSE float32)
-    rq, rk, rv = orc.attention_bwd(q, k, v, o.double().cpu().numpy(), lse.double().cpu().numpy(), do, N,
+    # the backward on the saved state as stored (the oracle's O rounded to
+    # bf16, LSE to float32); the expected gradient uses that same state
+    o_bf = torch.from_numpy(ro).to(torch.bfloat16)
+    l_f = torch.from_numpy(rl).float()
+    dq, dk, dv = ra.bwd(dev["q"], dev["k"], dev["v"], o_bf.cuda(), l_f.cuda(), dev["do"], N, case["causal"],
+                        case["layout"])
+    torch.cuda.synchronize()
+    ra.check_device_status()
+    rq, rk, rv = orc.attention_bwd(q, k, v, o_bf.double().numpy(), l_f.double().numpy(), do, N,
                                    case["causal"], case["layout"])
     for g, r in ((dq, rq), (dk, rk), (dv, rv)):
         g = g.double().cpu().numpy()

@@ -46,6 +46,26 @@ def test_merge_matches_oracle(ra, dtype, D, tol_o):
     assert max_err(gla.cpu().numpy(), rl) <= 2e-6 * max(1.0, float(np.abs(rl).max()))
 
 
+@pytest.mark.parametrize("D,rows", [(128, 3000), (36, 511), (5, 100)])
+def test_merge_f32_state_bf16_partial(ra, D, rows):
+    """A float32 running state folding a bf16 partial (ring hosts keep their
+    output in float32 across rounds): both vectorised (D % 4 == 0) and scalar
+    paths, against the oracle's merge of the same rounded inputs."""
+    oa, la, ob, lb = _partials(rows, D, seed=100 + D)
+    ta = torch.from_numpy(oa).float()
+    tb = torch.from_numpy(ob).to(torch.bfloat16)
+    la32, lb32 = torch.from_numpy(la).float(), torch.from_numpy(lb).float()
+    la32[::9] = -float("inf")
+    lb32[::4] = -float("inf")
+    ro, rl = orc.lse_merge(ta.double().numpy(), la32.double().numpy(), tb.double().numpy(), lb32.double().numpy())
+    ga, gla = ta.cuda(), la32.cuda()
+    ra.merge(ga, gla, tb.cuda(), lb32.cuda())
+    torch.cuda.synchronize()
+    assert ga.dtype == torch.float32
+    assert max_err(ga.double().cpu().numpy(), ro) <= 1e-5
+    assert max_err(gla.cpu().numpy(), rl) <= 2e-6 * max(1.0, float(np.abs(rl[np.isfinite(rl)]).max()))
+
+
 def test_merge_edge_rows(ra):
     D = 16
     o_a = torch.arange(4 * D, dtype=torch.float32).view(4, D)

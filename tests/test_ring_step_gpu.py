@@ -68,6 +68,42 @@ def test_chained_steps_equal_fused_forward(ra, layout, causal):
         assert max_err(o.float().cpu().numpy(), o_full[:, :, sl].float().cpu().numpy()) <= TOL["bf16"]["o"]
 
 
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_chained_steps_32_blocks_float32_state(ra, layout):
+    """32 ring hosts (the block count of the 131072-token workload), each
+    chaining its 32 ring steps: with the running output kept in float32 and
+    every bf16 partial folded into it (what ring.ring_forward does), the
+    result matches the oracle at the forward's tolerance, and rounding the
+    state to bf16 after every round is never more accurate."""
+    B, H, N, c = 1, 2, 32, 128
+    inp = make_inputs(B, H, N * c, 128, seed=33)
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v")}
+    qb, kb, vb = (_blocks(dev[x], N) for x in ("q", "k", "v"))
+    q, k, v = (as_float64(inp[x]) for x in ("q", "k", "v"))
+    ro, rl = orc.naive_attention(q, k, v, N, True, layout)
+    err32 = err16 = 0.0
+    for i in range(N):
+        o32 = torch.zeros((B, H, c, 128), dtype=torch.float32, device="cuda")
+        l32 = torch.full((B, H, c), float("-inf"), dtype=torch.float32, device="cuda")
+        o16 = l16 = None
+        for j in orc.ring_order(i, N):
+            if layout == "contiguous" and j > i:
+                continue
+            oj, lj = ra.fwd_step(qb[i], kb[j], vb[j], N, i, j, True, layout)
+            ra.merge(o32, l32, oj, lj)
+            if o16 is None:
+                o16, l16 = oj.clone(), lj.clone()
+            else:
+                ra.merge(o16, l16, oj, lj)
+        torch.cuda.synchronize()
+        sl = slice(i * c, (i + 1) * c)
+        err32 = max(err32, max_err(o32.double().cpu().numpy(), ro[:, :, sl]))
+        err16 = max(err16, max_err(o16.double().cpu().numpy(), ro[:, :, sl]))
+        assert max_err(l32.cpu().numpy(), rl[:, :, sl]) <= TOL["bf16"]["lse"]
+    assert err32 <= TOL["bf16"]["o"], err32
+    assert err32 <= err16, (err32, err16)
+
+
 def _grad_tol(ref):
     return 2e-2 * max(1.0, float(np.abs(ref).max()))
 

@@ -2,8 +2,11 @@
 (for instance a plugin whose host framework owns all device memory, or a code
 path that must not call cudaMalloc because it can synchronise the device).
 
-It must give what ra_bwd gives with a caller-allocated workspace, call after
-call, while allocating nothing.  This file is collected last on purpose, so a
+It must give exactly what ra_bwd gives with a caller-allocated workspace,
+call after call, while allocating nothing.  The backward kernels are
+deterministic (every output row has one writer and no atomics), so the check is
+bit equality: a stale value left in the shared array by an earlier call would
+show up as a difference in even one row.  This file is collected last on purpose, so a
 run that stops at the first failure has run every other test first; it also
 passes on its own in a fresh process.
 """
@@ -13,15 +16,6 @@ import torch
 from ring_attention_fwd_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
-
-
-def _close(g, ref, name):
-    g, ref = g.double(), ref.double()
-    scale = max(1.0, float(ref.abs().max()))
-    err = float((g - ref).abs().max())
-    assert err <= 2e-2 * scale, f"{name}: max err {err:.3e}"
-    fro = float((g - ref).norm() / ref.norm().clamp_min(1e-30))
-    assert fro <= 1e-2, f"{name}: relative Frobenius {fro:.3e}"
 
 
 def test_no_alloc_backward_matches_workspace_backward():
@@ -49,7 +43,7 @@ def test_no_alloc_backward_matches_workspace_backward():
             if call == 1:              # the first call may load the library's module; later ones change nothing
                 assert torch.cuda.mem_get_info()[0] == free_before
             for name, g, r in zip(("dQ", "dK", "dV"), outs, ref):
-                _close(g, r, f"{name} (call {call}, {layout})")
+                assert torch.equal(g, r), f"{name} (call {call}, {layout}) differs from ra_bwd"
 
 
 def test_no_alloc_backward_rejects_too_large():
