@@ -72,6 +72,53 @@ def _src_hash(name: str) -> str:
     return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
+def _hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured copy bandwidth"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def merge_bandwidth(rows: int, D: int, launches: int = 20) -> dict:
+    """ra_merge at one ring round's size: `rows` rows of D, bf16 state and
+    partial, and a float32 state folding a bf16 partial (what ring_forward
+    does each round).  Every launch is timed alone with CUDA events after a
+    write of 512 MB has pushed the operands out of L2; the median is reported
+    against the measured HBM copy bandwidth.  Algorithmic bytes per row: read
+    both states and both LSEs, write the merged state and LSE."""
+    import torch
+    import ring_attention_fwd_gb300 as ra
+    hbm, hsrc = _hbm_peak()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    out = {"rows": rows, "D": D, "l2": "flushed before each launch (512 MB write)", "peak": hbm,
+           "peak_kind": hsrc, "launches": launches}
+    for name, adt, bdt in (("bf16", torch.bfloat16, torch.bfloat16), ("f32_state_bf16_partial", torch.float32,
+                                                                       torch.bfloat16)):
+        oa = torch.randn((rows, D), device="cuda", generator=g).to(adt)
+        ob = torch.randn((rows, D), device="cuda", generator=g).to(bdt)
+        la = torch.randn((rows,), device="cuda", generator=g)
+        lb = torch.randn((rows,), device="cuda", generator=g)
+        nbytes = rows * (2 * D * oa.element_size() + D * ob.element_size() + 12)
+        ms = []
+        for k in range(launches + 2):
+            flush.fill_(k & 0xff)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ra.merge(oa, la, ob, lb)
+            e1.record()
+            e1.synchronize()
+            if k >= 2:
+                ms.append(e0.elapsed_time(e1))
+        med = statistics.median(ms)
+        out[name] = {"bytes": nbytes, "ms": med, "gbps": nbytes / (med * 1e-3) / 1e9,
+                     "frac_of_hbm": nbytes / (med * 1e-3) / 1e9 / hbm}
+    ra.check_device_status()
+    return out
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -207,10 +254,16 @@ def link_times(stream, h2d, d2h) -> dict:
 
     bu = sum(src.numel() * src.element_size() for _, src in h2d)
     bd = sum(src.numel() * src.element_size() for _, src in d2h)
-    h_ms = min(timed(h2d, []) for _ in range(2))
-    d_ms = min(timed([], d2h) for _ in range(2))
-    b_ms = min(timed(h2d, d2h) for _ in range(2))
-    return {"h2d_ms": h_ms, "d2h_ms": d_ms, "both_ms": b_ms, "h2d_gbs": bu / h_ms / 1e6, "d2h_gbs": bd / d_ms / 1e6}
+    # three samples each, interleaved; the spread shows a slow outlier (a first
+    # touch, another tenant on the host link) instead of hiding it in a minimum
+    hs, ds, bs = [], [], []
+    for _ in range(3):
+        hs.append(timed(h2d, []))
+        ds.append(timed([], d2h))
+        bs.append(timed(h2d, d2h))
+    h_ms, d_ms, b_ms = (statistics.median(x) for x in (hs, ds, bs))
+    return {"h2d_ms": h_ms, "d2h_ms": d_ms, "both_ms": b_ms, "h2d_gbs": bu / h_ms / 1e6, "d2h_gbs": bd / d_ms / 1e6,
+            "stat": "median of 3", "h2d_ms_all": hs, "d2h_ms_all": ds, "both_ms_all": bs}
 
 
 def _dist():
@@ -369,37 +422,39 @@ def run_ours(args, w):
     ms_step = total_ms / args.steps
     value = f_step * ws / (ms_step * 1e-3) / 1e12
 
-    # end to end through the public API with host buffers: every step uploads
-    # its inputs from pinned memory and downloads every output, overlapped with
-    # the neighbouring steps' compute (double-buffered device tensors)
-    outs_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
-                 "lse": torch.empty_like(lse, device="cpu").pin_memory()}
-    if with_bwd:
-        for n in ("dq", "dk", "dv"):
-            outs_host[n] = torch.empty_like(dq, device="cpu").pin_memory()
-    in_names = ["q", "k", "v"] + (["do"] if with_bwd else [])
-    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
-    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
-    ins = [dev, {n: torch.empty_like(dev[n]) for n in in_names}]
-    outs = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
-            {"o": torch.empty_like(o), "lse": torch.empty_like(lse), "dq": torch.empty_like(dq),
-             "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)}]
-
-    def e2e_compute(b):
-        x, y = ins[b], outs[b]
-        ra.fwd(x["q"], x["k"], x["v"], N, causal, layout, o=y["o"], lse=y["lse"])
+    e2e_ms = link = None
+    if not args.kernels_only:
+        # end to end through the public API with host buffers: every step uploads
+        # its inputs from pinned memory and downloads every output, overlapped with
+        # the neighbouring steps' compute (double-buffered device tensors)
+        outs_host = {"o": torch.empty_like(o, device="cpu").pin_memory(),
+                     "lse": torch.empty_like(lse, device="cpu").pin_memory()}
         if with_bwd:
-            ra.bwd(x["q"], x["k"], x["v"], y["o"], y["lse"], x["do"], N, causal, layout, dq=y["dq"], dk=y["dk"],
-                   dv=y["dv"], workspace=work)
+            for n in ("dq", "dk", "dv"):
+                outs_host[n] = torch.empty_like(dq, device="cpu").pin_memory()
+        in_names = ["q", "k", "v"] + (["do"] if with_bwd else [])
+        h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
+        d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+        ins = [dev, {n: torch.empty_like(dev[n]) for n in in_names}]
+        outs = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
+                {"o": torch.empty_like(o), "lse": torch.empty_like(lse), "dq": torch.empty_like(dq),
+                 "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)}]
 
-    e2e_steps = max(8, args.steps)          # amortises the unhidden first upload and last download
-    e2e_ms = pipelined_e2e(e2e_steps, stream, lambda b: [(ins[b][n], host[n]) for n in in_names], e2e_compute,
-                           lambda b: [(outs_host[n], outs[b][n]) for n in outs_host])
-    link = link_times(stream, [(ins[1][n], host[n]) for n in in_names], [(outs_host[n], outs[0][n]) for n in outs_host])
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+        def e2e_compute(b):
+            x, y = ins[b], outs[b]
+            ra.fwd(x["q"], x["k"], x["v"], N, causal, layout, o=y["o"], lse=y["lse"])
+            if with_bwd:
+                ra.bwd(x["q"], x["k"], x["v"], y["o"], y["lse"], x["do"], N, causal, layout, dq=y["dq"], dk=y["dk"],
+                       dv=y["dv"], workspace=work)
+
+        e2e_steps = max(8, args.steps)          # amortises the unhidden first upload and last download
+        e2e_ms = pipelined_e2e(e2e_steps, stream, lambda b: [(ins[b][n], host[n]) for n in in_names], e2e_compute,
+                               lambda b: [(outs_host[n], outs[b][n]) for n in outs_host])
+        link = link_times(stream, [(ins[1][n], host[n]) for n in in_names], [(outs_host[n], outs[0][n]) for n in outs_host])
+        if ws > 1:
+            tt = torch.tensor([e2e_ms], device="cuda")
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
 
     burst, sustained, src = _peaks()
     # Algorithmic FLOPs per launch of each tensor-core kernel.  The backward's
@@ -410,12 +465,20 @@ def run_ours(args, w):
     algo = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 1 * gemm}
     executed = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 3 * gemm}
     kernels = {}
+    clocks = clk.summary()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
     for name, lst in per_kernel.items():
         mean_ms = statistics.mean(lst)
         kernels[name] = {"launches": len(lst), "ms": mean_ms}
         if name in algo:
             kernels[name]["tflops_algorithmic"] = algo[name] / (mean_ms * 1e-3) / 1e12
             kernels[name]["tflops_executed"] = executed[name] / (mean_ms * 1e-3) / 1e12
+            if clocks.get("sm_mhz"):
+                # per clock, apart from the power cap: executed FLOP over (cycles x SMs x the
+                # dense bf16 tensor rate of 8192 FLOP per clock per SM)
+                cyc = mean_ms * 1e-3 * clocks["sm_mhz"] * 1e6
+                kernels[name]["mcycles_at_median_clock"] = cyc / 1e6
+                kernels[name]["per_clock_frac"] = executed[name] / (cyc * sms * 8192)
     dom = max((n for n in kernels if n in algo), key=lambda n: kernels[n]["ms"])
     achieved = kernels[dom]["tflops_algorithmic"]
     src_file = {"fwd": "fwd_bf16.cu", "bwd_dkv": "bwd_bf16.cu", "bwd_dq": "bwd_bf16.cu"}[dom]
@@ -445,13 +508,16 @@ def run_ours(args, w):
                            "value_exact_tflops": fl.fwd_flops_exact(B, H, S, D, causal) * (3.5 if with_bwd else 1.0)
                            * ws / (ms_step * 1e-3) / 1e12},
         "roofline": roofline,
-        "e2e": {"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); double-buffered",
-                "link_alone": link},
+        "e2e": ({"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                 "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); "
+                           "double-buffered",
+                 "link_alone": link} if e2e_ms is not None else None),
         "kernels": kernels,
         "gpu_launches": len(ktimes),
-        "clocks": clk.summary(),
+        "clocks": clocks,
+        # one ring round's merge (a host's c query rows of every head), outside the timed region
+        "merge": None if args.kernels_only else merge_bandwidth(B * H * (S // N), D),
     }
     if rank == 0 and not args.no_cpu_baseline:
         cores = len(os.sched_getaffinity(0))
@@ -627,12 +693,15 @@ def run_decode(args, w):
     kernels = {n: {"launches": len(l), "ms": statistics.mean(l)} for n, l in per_kernel.items()}
     split_ms = kernels["decode_split"]["ms"]
     split_bytes = B * H * (2 * S * D * 2 + D * 2)          # reads q, K, V
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            hbm, hsrc = float(json.load(f)["hbm_gbs"]), "measured copy bandwidth"
-    except Exception:
-        hbm, hsrc = 6800.0, "fallback"
+    hbm, hsrc = _hbm_peak()
     achieved = split_bytes / (split_ms * 1e-3) / 1e9
+    # the combine reads every partial (the workspace: items x (D + 1) floats, padded to 256 B)
+    # and writes O (bf16) and LSE (f32) per head
+    comb = kernels.get("decode_combine")
+    if comb:
+        cb = ra.decode_workspace_bytes(B, H, S, D, N) + B * H * (2 * D + 4)
+        comb.update(bytes=cb, gbps=cb / (comb["ms"] * 1e-3) / 1e9, frac_of_hbm=cb / (comb["ms"] * 1e-3) / 1e9 / hbm,
+                    bound="latency: one CTA per head walks its partials serially")
     tr = NCU_TRAFFIC.get("decode_split")
     traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash("decode.cu") and \
         tr["workload"] == args.workload else None
@@ -838,6 +907,11 @@ def main():
     ap.add_argument("--workload", default="long_128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads instead of its own (same per-head shape; "
+                         "for profiling captures that must stay small)")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="time the kernels only: no end-to-end copies, merge or CPU baseline (profiling runs)")
     ap.add_argument("--balance", action="store_true",
                     help="report per-virtual-host work and time, striped vs contiguous (default workload balance_32k)")
     args = ap.parse_args()
@@ -858,6 +932,10 @@ def main():
         return
     from ring_attention_fwd_gb300.inputs import LONG_WORKLOADS
     w = dict(WORKLOADS[args.workload] if args.workload in WORKLOADS else LONG_WORKLOADS[args.workload])
+    if args.heads > 0:
+        w["H"] = args.heads
+    if args.kernels_only:
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -115,6 +115,30 @@ RA_API int ra_fwd_step(const void* Q_i, const void* K_j, const void* V_j,
            void* O, float* LSE, void* stream);
 
 /*
+ * ra_fwd_step_fold -- ra_fwd_step that folds its partial state into the
+ * host's running state instead of returning it ([CH] §5.2, one host and one
+ * round; the fold is the LogSumExp merge of [FT] "Online Softmax").  Per row:
+ *     lse = M + ln(e^{lse_acc-M} + e^{lse_j-M}),  M = max(lse_acc, lse_j);
+ *     O_acc <- e^{lse_acc-lse} O_acc + e^{lse_j-lse} O_j,  LSE_acc <- lse,
+ * where (O_j, lse_j) is what ra_fwd_step would return.  It happens in the
+ * forward kernel's epilogue, one thread per row, so a round is one launch and
+ * the partial never leaves the chip in bf16.  Start a host's state at
+ * LSE_acc = -inf (such rows are empty: O_acc is not read there) and fold the
+ * N rounds in any order; the result is that host's rows of ra_fwd in float32.
+ * Rows that see none of block j's keys are left unchanged, and a contiguous
+ * causal round j > i launches nothing.
+ *
+ *   Q_i, K_j, V_j : [B,H,c,128] bf16 (dtype must be RA_BF16).
+ *   O_acc : [B,H,c,128] float32, 16-byte aligned (in/out);
+ *   LSE_acc : [B,H,c] float32 (in/out).  Other arguments as ra_fwd_step.
+ * Errors: RA_ERR_ARG (null pointer, misalignment, indices, sizes),
+ * RA_ERR_UNSUPPORTED (dtype other than bf16, D != 128), RA_ERR_CUDA.
+ */
+RA_API int ra_fwd_step_fold(const void* Q_i, const void* K_j, const void* V_j, int64_t B, int64_t H, int64_t c,
+                            int64_t D, int64_t N, int64_t i, int64_t j, int causal, int layout, int dtype,
+                            float* O_acc, float* LSE_acc, void* stream);
+
+/*
  * ra_merge -- LogSumExp merge of two partial states over disjoint key sets,
  * in place into (O_a, lse_a)  ([FT] "Online Softmax": l = l1 e^{m1-m} +
  * l2 e^{m2-m} and its log-space form).  Per row:

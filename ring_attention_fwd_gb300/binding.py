@@ -32,6 +32,8 @@ SIGNATURES = {
     "ra_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp, _vp]),
     "ra_fwd_step": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp, _fp,
                            _vp]),
+    "ra_fwd_step_fold": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _fp,
+                                _fp, _vp]),
     "ra_merge": (_int, [_vp, _fp, _vp, _fp, _i64, _i64, _int, _vp]),
     "ra_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64]),
     "ra_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
@@ -194,6 +196,23 @@ def fwd_step(q_i, k_j, v_j, n_blocks: int, i: int, j: int, causal: bool = True, 
                              int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype], o.data_ptr(),
                              lse.data_ptr(), _stream_ptr(stream)))
     return o, lse
+
+
+def fwd_step_fold(q_i, k_j, v_j, n_blocks: int, i: int, j: int, causal: bool = True, layout: str = "contiguous",
+                  *, o_acc, lse_acc, stream=None):
+    """One ring step of host i folded into its running state: the partial of
+    query block q_i [B, H, c, 128] (bf16) over KV block j is LogSumExp-merged
+    in place into o_acc [B, H, c, 128] and lse_acc [B, H, c] (float32).
+    Start a host's state with lse_acc = -inf.  Returns (o_acc, lse_acc)."""
+    B, H, c, D = _need_4d(q_i, "q_i")
+    for name, t in (("k_j", k_j), ("v_j", v_j)):
+        _need(t, name, q_i.dtype, q_i.shape, q_i.device)
+    _need(o_acc, "o_acc", torch.float32, q_i.shape, q_i.device)
+    _need(lse_acc, "lse_acc", torch.float32, (B, H, c), q_i.device)
+    _check(lib().ra_fwd_step_fold(q_i.data_ptr(), k_j.data_ptr(), v_j.data_ptr(), B, H, c, D, int(n_blocks), int(i),
+                                  int(j), int(bool(causal)), _LAYOUT[layout], _DTYPE[q_i.dtype], o_acc.data_ptr(),
+                                  lse_acc.data_ptr(), _stream_ptr(stream)))
+    return o_acc, lse_acc
 
 
 def merge(o_a, lse_a, o_b, lse_b, *, stream=None):

@@ -39,7 +39,7 @@ enum : int {
 
 // Check sites (CheckRec::first_site): kernel in the high byte, access below.
 enum : unsigned int {
-  SITE_FWD_TMA_Q = 0x101, SITE_FWD_TMA_K, SITE_FWD_TMA_V, SITE_FWD_O, SITE_FWD_LSE,
+  SITE_FWD_TMA_Q = 0x101, SITE_FWD_TMA_K, SITE_FWD_TMA_V, SITE_FWD_O, SITE_FWD_LSE, SITE_FWD_FOLD,
   SITE_F32_Q = 0x201, SITE_F32_KV, SITE_F32_O, SITE_F32_LSE,
   SITE_PREP_IN = 0x301, SITE_PREP_LSE, SITE_PREP_OUT,
   SITE_DKV_TMA_Q = 0x401, SITE_DKV_TMA_DO, SITE_DKV_TMA_KV, SITE_DKV_VEC, SITE_DKV_OUT,

@@ -156,6 +156,8 @@ struct FwdArgs {
   int num_sms;
   cudaEvent_t* ev;             // null, or 2 events recorded before/after the kernel
   CheckRec* chk;               // per-device check record (used by the checked build only)
+  float* O_acc = nullptr;      // bf16 kernel, fold mode: running float32 state [B,H,S,D] and its
+  float* LSE_acc = nullptr;    //   LSE [B,H,S], merged with this call's partial instead of writing O, LSE
 };
 cudaError_t launch_fwd_f32(const FwdArgs& a);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tmap_k,

@@ -79,6 +79,8 @@ struct Params {
   int withhold_first_q;            // test aid: never load the first unit's Q (waits then time out)
   int64_t BH;                      // heads (B*H): extent of the tensors' third TMA dimension
   CheckRec* chk;
+  float* O_acc;                    // fold mode (non-null): running float32 state, merged in place
+  float* LSE_acc;
 };
 
 // K-major operand tile (rows x 128 cols bf16, two 128B-swizzled 64-col boxes):
@@ -397,6 +399,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       bool valid = rq < g.c;
       const int64_t grow_idx = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      if (p.O_acc) {
+        // Fold mode: LogSumExp-merge this call's partial (O = acc / l, lse_b) into the row of the
+        // running float32 state, which this thread alone owns.  A state row with LSE -inf is
+        // empty and is not read; a partial with no visible key leaves the row as it is.
+        if (valid && !(RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, grow_idx * HD, HD, p.BH * p.S * HD) &&
+                       RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, grow_idx, 1, p.BH * p.S)))
+          valid = false;
+        const float lse_b = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
+        const float lse_a = valid ? p.LSE_acc[grow_idx] : -INFINITY;
+        const bool fold = valid && lse_b != -INFINITY;
+        float wa = 0.f, wb = 0.f, lse_n = lse_a;
+        if (fold) {
+          const float M = fmaxf(lse_a, lse_b);
+          const float ea = expf(lse_a - M), eb = expf(lse_b - M);
+          lse_n = M + logf(ea + eb);
+          wa = ea / (ea + eb);
+          wb = eb / (ea + eb) * inv_l;   // the partial's O is acc * inv_l
+        }
+        float* srow = p.O_acc + grow_idx * HD;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t ov[32];
+          tmem_ld32(tO + ch * 32, ov);
+          tmem_ld_wait();
+          if (fold) {
+            float4* dst = reinterpret_cast<float4*>(srow + ch * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 a = lse_a == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[v4];
+              a.x = fmaf(wb, __uint_as_float(ov[4 * v4]), wa * a.x);
+              a.y = fmaf(wb, __uint_as_float(ov[4 * v4 + 1]), wa * a.y);
+              a.z = fmaf(wb, __uint_as_float(ov[4 * v4 + 2]), wa * a.z);
+              a.w = fmaf(wb, __uint_as_float(ov[4 * v4 + 3]), wa * a.w);
+              dst[v4] = a;
+            }
+          }
+        }
+        if (fold) p.LSE_acc[grow_idx] = lse_n;
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty[q]);
+        continue;
+      }
       __nv_bfloat16* orow = p.O + grow_idx * HD;
       if (valid && !RA_CHECK_RANGE(p.chk, SITE_FWD_O, grow_idx * HD, HD, p.BH * p.S * HD)) valid = false;
 #pragma unroll
@@ -453,6 +497,8 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   p.withhold_first_q = a.withhold_first_q;
   p.BH = a.B * a.H;
   p.chk = a.chk;
+  p.O_acc = a.O_acc;
+  p.LSE_acc = a.LSE_acc;
   {
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(fwd_kernel), SMEM_BYTES);
     if (e != cudaSuccess) return e;

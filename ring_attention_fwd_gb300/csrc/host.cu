@@ -180,15 +180,20 @@ int check_enums(int causal, int layout, int dtype) {
 // Validates and launches one forward over tensors of S rows cut into N blocks.
 // `strict` and `use_timing` serve ra_fwd_step (one block pair as a 1-block call).
 int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, int64_t S, int64_t D, int64_t N,
-             int causal, int layout, int dtype, void* O, float* LSE, void* stream, int strict, bool use_timing) {
-  if (!Q || !K || !V || !O || !LSE) return fail(RA_ERR_ARG, "ra_fwd: null pointer");
+             int causal, int layout, int dtype, void* O, float* LSE, void* stream, int strict, bool use_timing,
+             float* O_acc = nullptr, float* LSE_acc = nullptr) {
+  const bool fold = O_acc != nullptr;
+  if (!Q || !K || !V || (fold ? !LSE_acc : (!O || !LSE))) return fail(RA_ERR_ARG, "ra_fwd: null pointer");
+  if (fold && (!aligned(O_acc, 16) || !aligned(LSE_acc, 4)))
+    return fail(RA_ERR_ARG, "ra_fwd_step_fold: O_acc must be 16-byte and LSE_acc 4-byte aligned");
   int rc = check_sizes(B, H, S, D, N);
   if (rc != RA_OK) return rc;
   if ((rc = check_enums(causal, layout, dtype)) != RA_OK) return rc;
-  if (!aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd: LSE must be 4-byte aligned");
+  if (!fold && !aligned(LSE, 4)) return fail(RA_ERR_ARG, "ra_fwd: LSE must be 4-byte aligned");
+  if (fold && dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_fwd_step_fold: only the bf16 path folds");
   if (dtype == RA_BF16) {
     if (D != 128) return fail(RA_ERR_UNSUPPORTED, "ra_fwd: bf16 path needs D == 128 (got %lld)", (long long)D);
-    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16))
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || (!fold && !aligned(O, 16)))
       return fail(RA_ERR_ARG, "ra_fwd: bf16 tensors must be 16-byte aligned");
   } else {
     if (D % 4 != 0 || D > 128)
@@ -216,6 +221,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
   a.num_sms = d->num_sms;
   a.ev = kt_begin(RA_CALL_FWD, 1);
   a.chk = d->chk;
+  a.O_acc = O_acc;
+  a.LSE_acc = LSE_acc;
   cudaError_t e;
   if (dtype == RA_BF16) {
     CUtensorMap mq, mk, mv;
@@ -379,6 +386,28 @@ int ra_fwd_step(const void* Q_i, const void* K_j, const void* V_j, int64_t B, in
   const int pair_causal = (causal && (striped || j == i)) ? 1 : 0;
   const int strict = (causal && striped && j > i) ? 1 : 0;
   return fwd_impl(Q_i, K_j, V_j, B, H, c, D, 1, pair_causal, layout, dtype, O, LSE, stream, strict, false);
+}
+
+int ra_fwd_step_fold(const void* Q_i, const void* K_j, const void* V_j, int64_t B, int64_t H, int64_t c,
+                     int64_t D, int64_t N, int64_t i, int64_t j, int causal, int layout, int dtype, float* O_acc,
+                     float* LSE_acc, void* stream) {
+  if (N < 1 || i < 0 || i >= N || j < 0 || j >= N)
+    return fail(RA_ERR_ARG, "ra_fwd_step_fold: need 0 <= i, j < N (i=%lld j=%lld N=%lld)", (long long)i,
+                (long long)j, (long long)N);
+  int rc = check_enums(causal, layout, dtype);
+  if (rc != RA_OK) return rc;
+  if (!Q_i || !K_j || !V_j || !O_acc || !LSE_acc) return fail(RA_ERR_ARG, "ra_fwd_step_fold: null pointer");
+  const bool striped = layout == RA_STRIPED;
+  if (causal && !striped && j > i) {
+    // Every key of block j comes after every query of block i: nothing to fold.
+    if ((rc = check_sizes(B, H, c, D, 1)) != RA_OK) return rc;
+    if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "ra_fwd_step_fold: only the bf16 path folds");
+    return RA_OK;
+  }
+  const int pair_causal = (causal && (striped || j == i)) ? 1 : 0;
+  const int strict = (causal && striped && j > i) ? 1 : 0;
+  return fwd_impl(Q_i, K_j, V_j, B, H, c, D, 1, pair_causal, layout, dtype, nullptr, nullptr, stream, strict, false,
+                  O_acc, LSE_acc);
 }
 
 int ra_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows, int64_t D, int dtype,

@@ -11,7 +11,9 @@ states are folded with the LogSumExp merge.  Contiguous causal rounds whose
 block lies entirely in the future (j > i) are skipped (the block is still
 forwarded).
 
-The block compute and the merge default to the library's ``fwd_step`` and
+The block compute and the merge default to the library's ``fwd_step_fold``
+(bf16: each round's partial is merged into the float32 running state inside
+the forward kernel's epilogue, one launch per round) or ``fwd_step`` and
 ``merge`` (CUDA tensors, NCCL process group).  Both are parameters, so the
 exchange protocol can be exercised elsewhere with other implementations.
 
@@ -54,7 +56,13 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
     """
     n = dist.get_world_size(group)
     i = dist.get_rank(group)
-    if step is None or merge is None:
+    fold = None
+    if step is None and merge is None and q.dtype == torch.bfloat16:
+        from . import binding
+
+        def fold(qq, kk, vv, nn, ii, jj, oo, ll):
+            binding.fwd_step_fold(qq, kk, vv, nn, ii, jj, causal, layout, o_acc=oo, lse_acc=ll)
+    elif step is None or merge is None:
         from . import binding
         step = step or (lambda qq, kk, vv, nn, ii, jj: binding.fwd_step(qq, kk, vv, nn, ii, jj, causal, layout))
         merge = merge or (lambda o, l, oj, lj: binding.merge(o, l, oj, lj))
@@ -74,8 +82,11 @@ def ring_forward(q, k, v, *, causal: bool = True, layout: str = "contiguous", gr
                    dist.P2POp(dist.isend, cur_v, send_to, group), dist.P2POp(dist.irecv, nv, recv_from, group)]
             reqs = dist.batch_isend_irecv(ops)
         if not (causal and layout == "contiguous" and j > i):
-            oj, lj = step(q, cur_k, cur_v, n, i, j)
-            merge(o, lse, oj, lj)
+            if fold is not None:
+                fold(q, cur_k, cur_v, n, i, j, o, lse)
+            else:
+                oj, lj = step(q, cur_k, cur_v, n, i, j)
+                merge(o, lse, oj, lj)
         for r in reqs:
             ok = r.wait(datetime.timedelta(seconds=timeout_s)) if timeout_s is not None else r.wait()
             if ok is False:

@@ -33,7 +33,7 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     assert declared_symbols() == sorted([
-        "ra_fwd", "ra_fwd_step", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
+        "ra_fwd", "ra_fwd_step", "ra_fwd_step_fold", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
         "ra_decode_workspace_bytes", "ra_decode", "ra_ffn_workspace_bytes", "ra_ffn", "ra_set_timing_buffer",
         "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status",
         "ra_read_checks", "ra_last_error", "ra_version"])
@@ -252,3 +252,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no non-CUDA fallback"):
         binding.lib()
+
+
+def test_fwd_step_fold_rejects_bad_arguments(L):
+    def call(**kw):
+        a = dict(Q=FAKE, K=FAKE, V=FAKE, B=1, H=1, c=128, D=128, N=4, i=1, j=0, causal=1, layout=0, dtype=1,
+                 O=FAKE, L=FAKE)
+        a.update(kw)
+        return L.ra_fwd_step_fold(a["Q"], a["K"], a["V"], a["B"], a["H"], a["c"], a["D"], a["N"], a["i"], a["j"],
+                                  a["causal"], a["layout"], a["dtype"], a["O"], a["L"], None)
+    assert call(O=None) == 1 and "null" in L.ra_last_error().decode()
+    assert call(L=None) == 1
+    assert call(i=4) == 1 and "0 <= i, j < N" in L.ra_last_error().decode()
+    assert call(j=-1) == 1
+    assert call(dtype=0, i=0, j=3) == 2          # contiguous causal j > i: sizes and dtype still checked
+    assert call(i=0, j=3) == 0                   # ... and then nothing to fold, no launch
+    assert call(O=FAKE + 4) == 1 and "16-byte" in L.ra_last_error().decode()

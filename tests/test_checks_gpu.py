@@ -103,6 +103,15 @@ def test_checked_ring_steps_and_merge(ra):
             ro, rl = orc.block_pair_attention(q[0, h], k[0, h], v[0, h], i, j, N, True, layout)
             assert max_err(o[0, h].double().cpu().numpy(), ro) <= TOL["bf16"]["o"]
             assert max_err(lse[0, h].double().cpu().numpy(), rl) <= TOL["bf16"]["lse"]
+        o_acc = torch.zeros((B, H, c, 128), dtype=torch.float32, device="cuda")
+        l_acc = torch.full((B, H, c), float("-inf"), dtype=torch.float32, device="cuda")
+        ra.fwd_step_fold(blk(inp["q"], i), blk(inp["k"], j), blk(inp["v"], j), N, i, j, True, layout, o_acc=o_acc,
+                         lse_acc=l_acc)
+        _clean(ra, f"fwd_step_fold {i},{j}", need_boxes=True)
+        for h in range(H):
+            ro, rl = orc.block_pair_attention(q[0, h], k[0, h], v[0, h], i, j, N, True, layout)
+            assert max_err(o_acc[0, h].double().cpu().numpy(), ro) <= TOL["bf16"]["o"]
+            assert max_err(l_acc[0, h].double().cpu().numpy(), rl) <= TOL["bf16"]["lse"]
         acc = [torch.zeros((B, H, c, 128), dtype=torch.float32, device="cuda") for _ in range(3)]
         o_full, lse_full = ra.fwd(*(inp[x].cuda() for x in ("q", "k", "v")), N, True, layout)
         ra.read_checks()

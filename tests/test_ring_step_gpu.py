@@ -104,6 +104,54 @@ def test_chained_steps_32_blocks_float32_state(ra, layout):
     assert err32 <= err16, (err32, err16)
 
 
+@pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("striped", False)])
+def test_fold_chain_32_blocks(ra, layout, causal):
+    """ra_fwd_step_fold: every host folds its 32 rounds, in ring order, into a
+    float32 state inside the forward epilogue; the state equals the oracle's
+    rows at the forward's tolerance, and agrees with the step + merge chain."""
+    B, H, N, c = 1, 2, 32, 128
+    inp = make_inputs(B, H, N * c, 128, seed=34)
+    dev = {x: inp[x].cuda() for x in ("q", "k", "v")}
+    qb, kb, vb = (_blocks(dev[x], N) for x in ("q", "k", "v"))
+    q, k, v = (as_float64(inp[x]) for x in ("q", "k", "v"))
+    ro, rl = orc.naive_attention(q, k, v, N, causal, layout)
+    for i in range(N):
+        o = torch.full((B, H, c, 128), float("nan"), dtype=torch.float32, device="cuda")   # never read while empty
+        lse = torch.full((B, H, c), float("-inf"), dtype=torch.float32, device="cuda")
+        o2 = torch.zeros_like(o)
+        l2 = lse.clone()
+        for j in orc.ring_order(i, N):
+            ra.fwd_step_fold(qb[i], kb[j], vb[j], N, i, j, causal, layout, o_acc=o, lse_acc=lse)
+            oj, lj = ra.fwd_step(qb[i], kb[j], vb[j], N, i, j, causal, layout)
+            ra.merge(o2, l2, oj, lj)
+        torch.cuda.synchronize()
+        ra.check_device_status()
+        sl = slice(i * c, (i + 1) * c)
+        assert max_err(o.double().cpu().numpy(), ro[:, :, sl]) <= TOL["bf16"]["o"], i
+        assert max_err(lse.cpu().numpy(), rl[:, :, sl]) <= TOL["bf16"]["lse"], i
+        assert max_err(o.cpu().numpy(), o2.cpu().numpy()) <= TOL["bf16"]["o"], i
+
+
+def test_fold_leaves_unseen_rows_and_empty_rounds_alone(ra):
+    """A contiguous causal round j > i folds nothing; a striped round j > i
+    hides each query's own row, so row 0 of block i sees no key of block j and
+    its state stays bit-identical."""
+    B, H, N, c = 1, 1, 4, 128
+    inp = make_inputs(B, H, N * c, 128, seed=35)
+    qb, kb, vb = (_blocks(inp[x].cuda(), N) for x in ("q", "k", "v"))
+    g = torch.Generator().manual_seed(3)
+    o = torch.randn((B, H, c, 128), generator=g).cuda()
+    lse = torch.randn((B, H, c), generator=g).cuda()
+    o0, l0 = o.clone(), lse.clone()
+    ra.fwd_step_fold(qb[1], kb[3], vb[3], N, 1, 3, True, "contiguous", o_acc=o, lse_acc=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o0) and torch.equal(lse, l0)
+    ra.fwd_step_fold(qb[1], kb[3], vb[3], N, 1, 3, True, "striped", o_acc=o, lse_acc=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o[0, 0, 0], o0[0, 0, 0]) and torch.equal(lse[0, 0, 0], l0[0, 0, 0])
+    assert not torch.equal(o[0, 0, 1:], o0[0, 0, 1:])
+
+
 def _grad_tol(ref):
     return 2e-2 * max(1.0, float(np.abs(ref).max()))
 
