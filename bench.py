@@ -58,8 +58,8 @@ NCU_TRAFFIC = {
     "fwd": {"sha256": "045f5236731c288193c86cecf3fb9a472a9b659f54307f603a3ffdb7d892ee9a", "workload": "long_128k", "bytes_per_launch": (19.252 + 1.185) * 1e9},
     "bwd_dkv": {"sha256": "d03ea06215ec696de34c38fc93a4a393d6bdc5cc52cdd0f6c1718dbe747535dd", "workload": "long_128k", "bytes_per_launch": (12.889 + 2.137) * 1e9},
     "bwd_dq": {"sha256": "d03ea06215ec696de34c38fc93a4a393d6bdc5cc52cdd0f6c1718dbe747535dd", "workload": "long_128k", "bytes_per_launch": (9.834 + 1.070) * 1e9},
-    "decode_split": {"sha256": "733ad39ef4633cbd9d703ea228e16e39d31daa93ce6adae96fedd2757bea1600", "workload": "decode_256k", "bytes_per_launch": 4295065088 + 6632448},
-    "ffn_up": {"sha256": "aa92e7b87505de12e91fcef22a3f61e267b872092e1256658477a35c5218c8fe", "workload": "ffn_7b", "bytes_per_launch": (220.352 + 80.051) * 1e6},
+    "decode_split": {"sha256": "db519d009c6e14d06bbde7b8df9ec6dab5ec5aeb1dc7cbff5fa4dc7eeea7a5b8", "workload": "decode_256k", "bytes_per_launch": 4295068000 + 6642688},
+    "ffn_up": {"sha256": "e3c1fddde6a2bcd126b3ceb1de1f6d6f977d1cc7e45d80e1a639318de4a2afb1", "workload": "ffn_7b", "bytes_per_launch": (218.333 + 79.864) * 1e6},
 }
 
 
@@ -119,6 +119,42 @@ def merge_bandwidth(rows: int, D: int, launches: int = 20) -> dict:
     return out
 
 
+def ring_round(dev: dict, N: int, causal: bool, layout: str, launches: int = 10) -> dict:
+    """One ring round at the workload's block size (host N-1 against block 0,
+    every key visible): the step folded into a float32 state in the kernel's
+    epilogue (ra_fwd_step_fold) against the step writing its partial and a
+    separate merge into the same state.  Median of `launches` each."""
+    import torch
+    import ring_attention_fwd_gb300 as ra
+    B, H, S, D = dev["q"].shape
+    c = S // N
+    qi = dev["q"][:, :, (N - 1) * c:].contiguous()
+    kj, vj = dev["k"][:, :, :c].contiguous(), dev["v"][:, :, :c].contiguous()
+    o_acc = torch.zeros((B, H, c, D), dtype=torch.float32, device="cuda")
+    l_acc = torch.zeros((B, H, c), dtype=torch.float32, device="cuda")
+    oj, lj = torch.empty_like(qi), torch.empty_like(l_acc)
+
+    def timed(fn):
+        ms = []
+        for k in range(launches + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            if k >= 2:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    fold = timed(lambda: ra.fwd_step_fold(qi, kj, vj, N, N - 1, 0, causal, layout, o_acc=o_acc, lse_acc=l_acc))
+    step = timed(lambda: ra.fwd_step(qi, kj, vj, N, N - 1, 0, causal, layout, o=oj, lse=lj))
+    both = timed(lambda: (ra.fwd_step(qi, kj, vj, N, N - 1, 0, causal, layout, o=oj, lse=lj),
+                          ra.merge(o_acc, l_acc, oj, lj)))
+    ra.check_device_status()
+    return {"rows": B * H * c, "fold_ms": fold, "step_ms": step, "step_then_merge_ms": both,
+            "fold_saves": 1.0 - fold / both}
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -174,7 +210,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list) -> float:
+def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list, warmup: int = 2) -> float:
     """End-to-end loop with the host<->device copies overlapped with compute,
     as a training or serving loop prefetches: one copy stream uploads step
     k+1's inputs and another downloads step k's results (both directions of
@@ -186,6 +222,8 @@ def pipelined_e2e(steps: int, stream, h2d_list, compute, d2h_list) -> float:
     compute(b): one step on set b, on the current stream.
     Returns ms per step, CUDA events from the first upload to the last download."""
     import torch
+    if warmup:
+        pipelined_e2e(warmup, stream, h2d_list, compute, d2h_list, warmup=0)   # untimed
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -518,6 +556,7 @@ def run_ours(args, w):
         "clocks": clocks,
         # one ring round's merge (a host's c query rows of every head), outside the timed region
         "merge": None if args.kernels_only else merge_bandwidth(B * H * (S // N), D),
+        "ring_round": None if args.kernels_only else ring_round(dev, N, causal, layout),
     }
     if rank == 0 and not args.no_cpu_baseline:
         cores = len(os.sched_getaffinity(0))

@@ -292,6 +292,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       if (u >= p.num_units) break;
       const Unit w = unit_at(g, u);
       const int rq = w.r0 + q * BM + row;  // row inside query block i
+      float fold_lse_a = -INFINITY;        // fold mode: the state row's LSE, read while the unit runs
+      if (p.O_acc && rq < g.c) {           // and its O row brought into L2 for the unit's end
+        const int64_t gi = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
+        const char* srow = reinterpret_cast<const char*>(p.O_acc + gi * HD);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + 128 * k));
+        if (RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, gi, 1, p.BH * p.S)) fold_lse_a = p.LSE_acc[gi];
+      }
       float m_use = -INFINITY, l = 0.f;
       int t = 0, s_prev = -1;
       uint64_t t_step0 = 0;
@@ -407,7 +415,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                        RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, grow_idx, 1, p.BH * p.S)))
           valid = false;
         const float lse_b = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
-        const float lse_a = valid ? p.LSE_acc[grow_idx] : -INFINITY;
+        const float lse_a = valid ? fold_lse_a : -INFINITY;
         const bool fold = valid && lse_b != -INFINITY;
         float wa = 0.f, wb = 0.f, lse_n = lse_a;
         if (fold) {
@@ -417,17 +425,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           wa = ea / (ea + eb);
           wb = eb / (ea + eb) * inv_l;   // the partial's O is acc * inv_l
         }
-        float* srow = p.O_acc + grow_idx * HD;
+        float4* srow4 = reinterpret_cast<float4*>(p.O_acc + grow_idx * HD);
+        const bool read_a = fold && lse_a != -INFINITY;
+        // The state row streams through two register buffers: chunk ch + 1's eight 16-byte loads
+        // are in flight while chunk ch is combined and stored.
+        float4 st[2][8];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) st[0][v4] = read_a ? srow4[v4] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
+          if (ch + 1 < 4) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              st[(ch + 1) & 1][v4] = read_a ? srow4[(ch + 1) * 8 + v4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           uint32_t ov[32];
           tmem_ld32(tO + ch * 32, ov);
           tmem_ld_wait();
           if (fold) {
-            float4* dst = reinterpret_cast<float4*>(srow + ch * 32);
+            float4* dst = srow4 + ch * 8;
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4) {
-              float4 a = lse_a == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[v4];
+              float4 a = st[ch & 1][v4];
               a.x = fmaf(wb, __uint_as_float(ov[4 * v4]), wa * a.x);
               a.y = fmaf(wb, __uint_as_float(ov[4 * v4 + 1]), wa * a.y);
               a.z = fmaf(wb, __uint_as_float(ov[4 * v4 + 2]), wa * a.z);

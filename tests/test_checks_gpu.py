@@ -168,3 +168,43 @@ def test_checked_counts_forced_rescales(ra, B, H, S, N, causal, layout, mode):
     ro, rl = orc.naive_attention(q, k, as_float64(inp["v"]), N, causal, layout)
     assert max_err(o.double().cpu().numpy(), ro) <= TOL["bf16"]["o"]
     assert max_err(lse.double().cpu().numpy(), rl) <= TOL["bf16"]["lse"]
+
+
+def test_checked_build_full_size_workloads(ra):
+    """The largest extents the library meets in the specified workloads, with
+    every index and TMA box checked: the 131072-token forward and backward
+    (32 heads, 32 blocks), the 262144-token ring decode and the 7B-shaped
+    feedforward.  Zero violations, finite outputs (values are checked against
+    the oracle by the default build's tests)."""
+    from ring_attention_fwd_gb300.inputs import DECODE_WORKLOADS, FFN_WORKLOADS, WORKLOADS
+    w = WORKLOADS["long_128k"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    B, H, S, N = w["B"], w["H"], w["S"], w["N"]
+    q, k, v, do = (torch.randn((B, H, S, 128), device="cuda", generator=g).mul_(0.5).to(torch.bfloat16)
+                   for _ in range(4))
+    o, lse = ra.fwd(q, k, v, N, True, "contiguous")
+    r = _clean(ra, "131072-token forward", need_boxes=True)
+    assert bool(torch.isfinite(lse).all()) and bool(torch.isfinite(o.float()).all())
+    dq, dk, dv = ra.bwd(q, k, v, o, lse, do, N, True, "contiguous")
+    _clean(ra, "131072-token backward", need_boxes=True)
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t.float()).all())
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+    d = DECODE_WORKLOADS["decode_256k"]
+    qd = torch.randn((d["B"], d["H"], 128), device="cuda", generator=g).to(torch.bfloat16)
+    kc, vc = (torch.randn((d["B"], d["H"], d["S"], 128), device="cuda", generator=g).to(torch.bfloat16)
+              for _ in range(2))
+    od, ld = ra.decode(qd, kc, vc, d["N"])
+    _clean(ra, "262144-token decode")
+    assert bool(torch.isfinite(ld).all()) and bool(torch.isfinite(od.float()).all())
+    del kc, vc
+    f = FFN_WORKLOADS["ffn_7b"]
+    x = torch.randn((f["T"], f["h"]), device="cuda", generator=g).to(torch.bfloat16)
+    w1, w3 = (torch.randn((f["f"], f["h"]), device="cuda", generator=g).mul_(f["h"] ** -0.5).to(torch.bfloat16)
+              for _ in range(2))
+    w2 = torch.randn((f["h"], f["f"]), device="cuda", generator=g).mul_(f["f"] ** -0.5).to(torch.bfloat16)
+    y = ra.ffn(x, w1, w3, w2, f["block_rows"])
+    _clean(ra, "7B-shaped feedforward", need_boxes=True)
+    assert bool(torch.isfinite(y.float()).all())
