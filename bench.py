@@ -362,7 +362,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, **{k: w[k] for k in ("B", "H", "S", "D", "N", "causal", "layout")}},
+        "config": {"workload": args.workload, **{k: w[k] for k in ("B", "H", "S", "D", "N", "causal", "layout")},
+                   "input_scale": w["scale"], "step": "fwd+bwd"},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step: {desc}; numpy float64, BLAS threads = {cores}"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -382,6 +383,7 @@ def run_ours(args, w):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ra.set_fwd_kernel(args.fwd_kernel)
     B, H, S, D, N = w["B"], w["H"], w["S"], w["D"], w["N"]
     causal, layout = w["causal"], w["layout"]
     inp = make_inputs(B, H, S, D, w["seed"], dtype=w["dtype"], scale=w["scale"], with_grad=True)
@@ -443,12 +445,14 @@ def run_ours(args, w):
             step(True)
         t1.record(stream)
         torch.cuda.synchronize()
-    ktimes = ra.kernel_times()
+    ktimes = ra.kernel_times(with_clock=True)
     ra.set_kernel_timing(False)
     ra.check_device_status()
-    per_kernel = {}
-    for name, ms in ktimes:
+    per_kernel, kernel_mhz = {}, {}
+    for name, ms, mhz in ktimes:
         per_kernel.setdefault(name, []).append(ms)
+        if mhz > 0:
+            kernel_mhz.setdefault(name, []).append(mhz)
     total_ms = t0.elapsed_time(t1)
     if ws > 1:
         tt = torch.tensor([total_ms], device="cuda")
@@ -500,8 +504,8 @@ def run_ours(args, w):
     # the dK/dV kernel and one (dQ) in the dQ kernel, which also recomputes S
     # and dP (executed: three GEMMs).
     gemm = f_fwd / 2
-    algo = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 1 * gemm}
-    executed = {"fwd": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 3 * gemm}
+    algo = {"fwd": f_fwd, "fwd_pair": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 1 * gemm}
+    executed = {"fwd": f_fwd, "fwd_pair": f_fwd, "bwd_dkv": 4 * gemm, "bwd_dq": 3 * gemm}
     kernels = {}
     clocks = clk.summary()
     sms = torch.cuda.get_device_properties(local).multi_processor_count
@@ -511,15 +515,23 @@ def run_ours(args, w):
         if name in algo:
             kernels[name]["tflops_algorithmic"] = algo[name] / (mean_ms * 1e-3) / 1e12
             kernels[name]["tflops_executed"] = executed[name] / (mean_ms * 1e-3) / 1e12
-            if clocks.get("sm_mhz"):
-                # per clock, apart from the power cap: executed FLOP over (cycles x SMs x the
-                # dense bf16 tensor rate of 8192 FLOP per clock per SM)
-                cyc = mean_ms * 1e-3 * clocks["sm_mhz"] * 1e6
-                kernels[name]["mcycles_at_median_clock"] = cyc / 1e6
+            # per clock, apart from the power cap: executed FLOP over (cycles x SMs x the
+            # dense bf16 tensor rate of 8192 FLOP per clock per SM).  The clock is the one
+            # the kernel itself measured (its first CTA's cycle counter against the global
+            # timer); nvidia-smi's median over the whole step is kept beside it for reference.
+            if name in kernel_mhz:
+                mhz = statistics.median(kernel_mhz[name])
+                cyc = mean_ms * 1e-3 * mhz * 1e6
+                kernels[name]["sm_mhz_in_kernel"] = mhz
+                kernels[name]["mcycles"] = cyc / 1e6
                 kernels[name]["per_clock_frac"] = executed[name] / (cyc * sms * 8192)
+            if clocks.get("sm_mhz"):
+                cyc = mean_ms * 1e-3 * clocks["sm_mhz"] * 1e6
+                kernels[name]["per_clock_frac_at_smi_median"] = executed[name] / (cyc * sms * 8192)
     dom = max((n for n in kernels if n in algo), key=lambda n: kernels[n]["ms"])
     achieved = kernels[dom]["tflops_algorithmic"]
-    src_file = {"fwd": "fwd_bf16.cu", "bwd_dkv": "bwd_bf16.cu", "bwd_dq": "bwd_bf16.cu"}[dom]
+    src_file = {"fwd": "fwd_bf16.cu", "fwd_pair": "fwd_bf16_pair.cu", "bwd_dkv": "bwd_bf16.cu",
+                "bwd_dq": "bwd_bf16.cu"}[dom]
     tr = NCU_TRAFFIC.get(dom)
     traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash(src_file) and \
         tr["workload"] == args.workload and args.heads == 0 else None
@@ -536,6 +548,7 @@ def run_ours(args, w):
                    "layout": layout, "input_scale": w["scale"], "step": "fwd+bwd" if with_bwd else "fwd only",
                    "l2": "inputs larger than L2 (1 GiB per tensor), no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "fwd_kernel": args.fwd_kernel,
         "fwd": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
                 "frac_of_peak": f_fwd / (fwd_ms * 1e-3) / 1e12 / sustained},
         "bwd": ({"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
@@ -951,6 +964,8 @@ def main():
                          "for profiling captures that must stay small)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="time the kernels only: no end-to-end copies, merge or CPU baseline (profiling runs)")
+    ap.add_argument("--fwd-kernel", default="single", choices=["single", "pair"],
+                    help="bf16 forward kernel: one CTA per SM (the library's default) or SM pairs")
     ap.add_argument("--balance", action="store_true",
                     help="report per-virtual-host work and time, striped vs contiguous (default workload balance_32k)")
     args = ap.parse_args()

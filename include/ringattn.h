@@ -336,13 +336,15 @@ RA_API int ra_set_timing_buffer(uint64_t* dev_buf, size_t n);
  * stream immediately before and after each kernel it launches; 0 turns it off
  * and drops unread records.  ra_kernel_times() waits for the recorded events,
  * writes one record per timed kernel (oldest call first) and releases them:
- *   call RA_CALL_FWD: kernel 0 = the forward kernel;
+ *   call RA_CALL_FWD: kernel 0 = the forward kernel (bf16 on one CTA per SM,
+ *                     or float32), kernel 1 = the bf16 forward on SM pairs
+ *                     (see ra_set_fwd_kernel);
  *   call RA_CALL_BWD: kernel 0 = preprocess (D_vec, LSE*log2e),
  *                     kernel 1 = dK/dV kernel, kernel 2 = dQ kernel.
  *   call RA_CALL_DECODE: kernel 0 = per-chunk partials, kernel 1 = combine;
  *   call RA_CALL_FFN: kernel 2b = gated up projection of block b, 2b+1 = its
  *                     down projection (calls of more than 8 blocks run untimed).
- * `ms` is the event-to-event time in milliseconds.  *count receives the number
+ * `ms` is the event-to-event time in milliseconds; `sm_mhz` as described below.  *count receives the number
  * of records; if it exceeds `capacity`, the first `capacity` are written, the
  * rest are dropped and RA_ERR_ARG is returned.  The library creates (and keeps
  * for reuse) the events; no device memory is allocated.
@@ -352,9 +354,30 @@ typedef struct {
   int call;     /* ra_call_kind */
   int kernel;   /* index inside the call, see above */
   float ms;     /* duration, or -1 if it could not be measured */
+  float sm_mhz; /* tensor-core kernels (bf16 forward, dK/dV, dQ): the SM clock
+                   the kernel ran at, from its first CTA's cycle counter over
+                   its own lifetime against the global nanosecond timer;
+                   -1 for the other kernels */
 } ra_kernel_time;
 RA_API int ra_set_kernel_timing(int enable);
 RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
+
+/*
+ * ra_set_fwd_kernel -- which kernel the bf16 forward (ra_fwd, ra_fwd_step,
+ * ra_fwd_step_fold) launches; a process-wide setting that applies to calls
+ * made after it returns, from any thread, on any device.  Both kernels compute
+ * the method's forward ("Ring Attention" explainer, aiqz.cc, §分块注意力: the
+ * same tiles, the same online-softmax update, in the same order) and give
+ * bit-identical results; they differ in how the GPU's SMs share the work:
+ *   RA_FWD_SINGLE (the default): one CTA per SM, work units of 256 query rows;
+ *   RA_FWD_PAIR: 2-CTA clusters on SM pairs, whose tensor-core MMAs span both
+ *                SMs (M = 256) so that each SM loads only half of every K and
+ *                V tile; work units of 512 query rows.  A call fails with
+ *                RA_ERR_UNSUPPORTED if the device cannot hold one such cluster.
+ * Returns RA_ERR_ARG for any other `kind`.  The float32 path is unaffected.
+ */
+typedef enum { RA_FWD_SINGLE = 0, RA_FWD_PAIR = 1 } ra_fwd_kernel;
+RA_API int ra_set_fwd_kernel(int kind);
 
 /*
  * ra_set_wait_test -- test aid for the bounded waits (no counterpart on the

@@ -50,6 +50,7 @@ SIGNATURES = {
     "ra_check_device_status": (_int, [_vp]),
     "ra_set_kernel_timing": (_int, [_int]),
     "ra_set_wait_test": (_int, [_int]),
+    "ra_set_fwd_kernel": (_int, [_int]),
     "ra_kernel_times": (_int, [_vp, _int, ctypes.POINTER(ctypes.c_int)]),
     "ra_read_checks": (_int, [_vp, _vp]),
     "ra_last_error": (ctypes.c_char_p, []),
@@ -371,6 +372,18 @@ def ffn(x, w1, w3, w2, block_rows: int, *, y=None, workspace=None, stream=None):
     return y
 
 
+FWD_KERNELS = {"single": 0, "pair": 1}
+
+
+def set_fwd_kernel(kind: str):
+    """Which kernel later bf16 forward calls launch: "single" (the default,
+    one CTA per SM) or "pair" (2-CTA clusters whose MMAs span an SM pair).
+    The two kernels give bit-identical results."""
+    if kind not in FWD_KERNELS:
+        raise ValueError(f"set_fwd_kernel: kind must be one of {sorted(FWD_KERNELS)}, got {kind!r}")
+    _check(lib().ra_set_fwd_kernel(FWD_KERNELS[kind]))
+
+
 def set_timing_buffer(buf):
     """Enable per-(virtual host, ring step) timing into a uint64/int64 CUDA
     tensor of >= N*N entries (caller zeroes it); None disables."""
@@ -382,10 +395,11 @@ def set_timing_buffer(buf):
 
 
 class KernelTime(ctypes.Structure):
-    _fields_ = [("call", ctypes.c_int), ("kernel", ctypes.c_int), ("ms", ctypes.c_float)]
+    _fields_ = [("call", ctypes.c_int), ("kernel", ctypes.c_int), ("ms", ctypes.c_float),
+                ("sm_mhz", ctypes.c_float)]
 
 
-KERNEL_NAMES = {(0, 0): "fwd", (1, 0): "bwd_prep", (1, 1): "bwd_dkv", (1, 2): "bwd_dq", (2, 0): "decode_split",
+KERNEL_NAMES = {(0, 0): "fwd", (0, 1): "fwd_pair", (1, 0): "bwd_prep", (1, 1): "bwd_dkv", (1, 2): "bwd_dq", (2, 0): "decode_split",
                 (2, 1): "decode_combine"}
 
 
@@ -395,13 +409,18 @@ def set_kernel_timing(enable: bool):
     _check(lib().ra_set_kernel_timing(int(bool(enable))))
 
 
-def kernel_times(capacity: int = 4096):
+def kernel_times(capacity: int = 4096, with_clock: bool = False):
     """Per-kernel durations of the calls timed since the last read: a list of
-    (name, ms), oldest first.  Waits for the recorded events."""
+    (name, ms), oldest first, or (name, ms, sm_mhz) with `with_clock` (the SM
+    clock a tensor-core kernel ran at, -1 for the others).  Waits for the
+    recorded events."""
     buf = (KernelTime * capacity)()
     n = ctypes.c_int(0)
     _check(lib().ra_kernel_times(ctypes.addressof(buf), capacity, ctypes.byref(n)))
-    return [(_kernel_name(buf[k].call, buf[k].kernel), buf[k].ms) for k in range(n.value)]
+    recs = [buf[k] for k in range(n.value)]
+    if with_clock:
+        return [(_kernel_name(r.call, r.kernel), r.ms, r.sm_mhz) for r in recs]
+    return [(_kernel_name(r.call, r.kernel), r.ms) for r in recs]
 
 
 def _kernel_name(call: int, kernel: int) -> str:

@@ -37,9 +37,10 @@
 // TMEM owner (the whole warp runs the issue loop so its operands stay
 // warp-uniform; one elected lane issues each tcgen05 instruction -- a single
 // issuing thread in a divergent branch reaches only ~2/3 of the tensor rate
-// with 128-wide MMAs), warps 4-7 and 8-11 the elementwise work, one thread per
-// TMEM lane (row); warpgroup g owns columns [64g, 64g+64) and writes its
-// packed bf16 results only over columns it has read.
+// with 128-wide MMAs), warps 2-9 the elementwise work, one thread per TMEM
+// lane (row): warp w reads lane quadrant w % 4 (the quadrant a warp may
+// address), warps 2-5 own columns [0, 64) and warps 6-9 columns [64, 128), and
+// each writes its packed bf16 results only over columns it has read.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -53,7 +54,7 @@ namespace bwd {
 
 constexpr int BT = 128;        // rows per KV tile and per query tile
 constexpr int HD = 128;
-constexpr int THREADS = 384;
+constexpr int THREADS = 320;
 constexpr uint32_t TILE_BYTES = BT * HD * 2;  // 32 KB
 constexpr uint32_t BOX_BYTES = TILE_BYTES / 2;
 constexpr uint32_t VEC_BYTES = BT * 4;
@@ -131,6 +132,7 @@ struct Params {
   int64_t BH;          // heads (B*H)
   int64_t vec_rows;    // rows of nlse2 / ndvec: BH * N * n_mb * 128
   CheckRec* chk;
+  unsigned long long* clk;   // clock record of this launch (kernel timing) or null
 };
 
 __device__ __forceinline__ int64_t vec_row(const RingGeom& g, int bh, int i, int qt) {
@@ -241,6 +243,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  clock_mark(p.clk, 0);
   // TMEM: dV [0,128) dK [128,256) S^T [256,384) dP^T [384,512); P^T is packed
   // (bf16) over S^T and dS^T over dP^T once each has been read.
   const uint32_t T_DV = tmem, T_DK = tmem + 128, T_S = tmem + 256, T_DP = tmem + 384;
@@ -395,9 +398,9 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------ P^T and dS^T, epilogue
-    const int grp = (warp - 4) >> 2;                     // query columns [64*grp, +64)
+    const int grp = (warp - 2) >> 2;                     // query columns [64*grp, +64)
     const int quad = warp & 3;
     const int t_row = quad * 32 + lane;                  // key row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -518,6 +521,7 @@ dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
   tc_fence_before();
   __syncthreads();
+  clock_mark(p.clk, 1);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -596,6 +600,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  clock_mark(p.clk, 0);
   // TMEM: dQ [0,128) Q [128,192) (bf16 rows, A operand) dS [192,256) (bf16, A operand)
   //       S [256,384) dP [384,512).  S and dP are free again as soon as they are
   //       in registers, so the next KV tile's S and dP MMAs overlap this tile's
@@ -740,9 +745,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       mma_commit_w(&bars->drain);
       mbar_drain(&bars->drain, 0, 200000000ull);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------- Q rows, dS, epilogue
-    const int grp = (warp - 4) >> 2;                     // key columns [64*grp, +64)
+    const int grp = (warp - 2) >> 2;                     // key columns [64*grp, +64)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                    // query row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -862,6 +867,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
 
   tc_fence_before();
   __syncthreads();
+  clock_mark(p.clk, 1);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -966,9 +972,11 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tm
   p.num_units = units;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
   if (a.ev) cudaEventRecord(a.ev[1], a.stream);
+  p.clk = a.clk_dkv;
   kv::dkv_kernel<<<grid, THREADS, kv::SMEM_BYTES, a.stream>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev) cudaEventRecord(a.ev[2], a.stream);
+  p.clk = a.clk_dq;
   q::dq_kernel<<<grid, THREADS, q::SMEM_BYTES, a.stream>>>(mk, mv, mdo, static_cast<const __nv_bfloat16*>(a.Q), p);
   e = cudaGetLastError();
   if (a.ev) cudaEventRecord(a.ev[3], a.stream);

@@ -70,7 +70,8 @@ __device__ __forceinline__ bool check_range(CheckRec* r, unsigned int site, long
 // tensor, and y below `ny`.  A load may start past the last row (the hardware
 // fills the box with zeros there), so callers pass as `ny` the exclusive bound
 // their schedule guarantees: S for tiles that start inside a block, S plus the
-// box height for a unit's second query tile.
+// rows by which a unit's later query tiles (or the upper half of a KV tile)
+// may start past it.
 __device__ __forceinline__ bool check_box(CheckRec* r, unsigned int site, int x, int y, int z, long long nx,
                                           long long ny, long long nz, int x_align) {
   atomicAdd(&r->events[EV_TMA_BOXES], 1ull);

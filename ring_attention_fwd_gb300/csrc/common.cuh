@@ -158,10 +158,18 @@ struct FwdArgs {
   CheckRec* chk;               // per-device check record (used by the checked build only)
   float* O_acc = nullptr;      // bf16 kernel, fold mode: running float32 state [B,H,S,D] and its
   float* LSE_acc = nullptr;    //   LSE [B,H,S], merged with this call's partial instead of writing O, LSE
+  unsigned long long* clk = nullptr;   // bf16 kernels: clock record (4 words) or null
 };
 cudaError_t launch_fwd_f32(const FwdArgs& a);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v);
+// The same forward on SM pairs (2-CTA clusters, cta_group::2 MMAs); `tmap_k64`
+// views K with 64-row boxes.
+cudaError_t launch_fwd_bf16_pair(const FwdArgs& a, const void* tmap_q, const void* tmap_k64,
+                                 const void* tmap_v);
+// How many 2-CTA clusters of the pair kernel the current device holds at once
+// (0: none fits; -1: the query failed).  Cached per device.
+int fwd_pair_clusters();
 // Operand types of the merge: state O_a / partial O_b.
 enum : int { MERGE_F32 = 0, MERGE_BF16 = 1, MERGE_F32_BF16 = 2 };
 cudaError_t launch_merge(void* O_a, float* lse_a, const void* O_b, const float* lse_b, int64_t rows,
@@ -189,6 +197,8 @@ struct BwdArgs {
   int num_sms;
   cudaEvent_t* ev;   // null, or 4 events: before prep, dK/dV and dQ kernels, and after
   CheckRec* chk;
+  unsigned long long* clk_dkv = nullptr;   // clock records (4 words) of the two main kernels, or null
+  unsigned long long* clk_dq = nullptr;
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, const void* tmap_q, const void* tmap_k,
                             const void* tmap_v, const void* tmap_do);

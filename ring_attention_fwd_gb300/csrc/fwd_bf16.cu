@@ -81,6 +81,7 @@ struct Params {
   CheckRec* chk;
   float* O_acc;                    // fold mode (non-null): running float32 state, merged in place
   float* LSE_acc;
+  unsigned long long* clk;         // clock record (kernel timing) or null
 };
 
 // K-major operand tile (rows x 128 cols bf16, two 128B-swizzled 64-col boxes):
@@ -136,6 +137,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  clock_mark(p.clk, 0);
   const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS};
   const int grid = gridDim.x;
   const int cta = blockIdx.x;
@@ -486,6 +488,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
   tc_fence_before();
   __syncthreads();
+  clock_mark(p.clk, 1);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -518,6 +521,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, const void* tmap_q, const void* tm
   p.chk = a.chk;
   p.O_acc = a.O_acc;
   p.LSE_acc = a.LSE_acc;
+  p.clk = a.clk;
   {
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(fwd_kernel), SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,596 @@
+// fwd_bf16_pair.cu -- the bf16 ring-order attention forward on SM pairs:
+// clusters of two CTAs whose tcgen05 MMAs run with cta_group::2 (M = 256).
+//
+// Method ("Ring Attention" explainer, aiqz.cc, §分块注意力 and §环状拓扑): the
+// same computation as fwd_bf16.cu -- query block i meets KV blocks
+// j = i, i-1, ... (mod N), each score tile S = Q_i K_j^T / sqrt(d) is folded
+// into per-row online-softmax state (m, l, O), contiguous causal blocks j > i
+// are skipped whole and diagonal tiles are masked per element (same page,
+// §工程实现).
+//
+// What the pair changes.  A work unit is 512 query rows of one head inside
+// one query block; CTA rank r of the pair owns rows [256r, 256r + 256) as two
+// 128-row tiles Q0, Q1 (the same ping-pong as the single-SM kernel).  Rank 0
+// issues every MMA for both: S_q = Q_q K^T and O_q += P_q V with M = 256
+// (128 rows from each CTA).  The B operand of a pair MMA is split in half
+// along N between the CTAs, so each CTA loads only half of every KV tile:
+// keys [64r, 64r + 64) of K (N of Q K^T is the key) and head-dim columns
+// [64r, 64r + 64) of V (N of P V is the head dim).  Per 128-key step a CTA
+// reads 32 KB instead of 64 KB, and the same shared memory holds a 6-stage K
+// ring and a 4-stage V ring instead of 3 and 2.
+//
+// Synchronisation across the pair:
+//   - both CTAs' TMA loads complete on rank 0's full barriers (rank 0 posts
+//     the pair's byte count); rank 0's MMA warp releases a stage to both
+//     producers with one commit per CTA;
+//   - S ready / O ready: one commit per CTA onto that CTA's barrier;
+//   - P ready / O drained: the 128 softmax threads of each CTA arrive on rank
+//     0's barrier (count 256), across the pair for rank 1, after waiting for
+//     their own TMEM stores or loads.
+// Every wait is bounded; a CTA that gives up also raises the other CTA's
+// abort flag, and both CTAs meet at a cluster barrier before TMEM is freed.
+// TMEM columns (each CTA): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace ra {
+namespace fwdp {
+
+constexpr int BM = 128;        // rows per Q tile (per CTA)
+constexpr int BN = 128;        // keys per KV step
+constexpr int HD = 128;        // head dim
+constexpr int UNIT_ROWS = 4 * BM;  // query rows per pair unit
+constexpr int KSTAGE = 6;
+constexpr int VSTAGE = 4;
+constexpr int THREADS = 320;
+constexpr uint32_t TILE_BYTES = BM * HD * 2;      // 32 KB: one Q tile
+constexpr uint32_t BOX_BYTES = TILE_BYTES / 2;    // 128 rows x 64 cols
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;   // this CTA's half of a K or V tile
+constexpr uint32_t KBOX_BYTES = HALF_BYTES / 2;   // 64 keys x 64 cols
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + KSTAGE * HALF_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGE * HALF_BYTES;
+constexpr uint32_t BAR_BYTES = 512;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units: p <= 2^8 between rescales
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+struct Bars {
+  uint64_t q_full, q_empty;                        // q_full: rank 0's counts the pair
+  uint64_t k_full[KSTAGE], k_empty[KSTAGE];        // *_full used on rank 0 only
+  uint64_t v_full[VSTAGE], v_empty[VSTAGE];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];  // p_full, o_empty: rank 0, count 256
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block");
+
+struct Params {
+  RingGeom g;
+  int S;
+  int64_t num_units;
+  float scale_log2;                // log2(e) / sqrt(D)
+  __nv_bfloat16* O;
+  float* LSE;
+  unsigned int* status;
+  unsigned long long* timing;      // [N*N] ns accumulators or null
+  int withhold_first_q;            // test aid: never load the first unit's Q (waits then time out)
+  int64_t BH;
+  CheckRec* chk;
+  float* O_acc;                    // fold mode (non-null): running float32 state, merged in place
+  float* LSE_acc;
+  unsigned long long* clk;         // clock record (kernel timing) or null
+};
+
+// Q tile (128 rows x 128 cols, two 128B-swizzled 64-col boxes), K-major A
+// operand: K-slice kk (16 columns).
+__device__ __forceinline__ uint64_t q_desc(uint32_t tile_saddr, int kk) {
+  return sdesc(tile_saddr + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024, SWZ_128B);
+}
+// This CTA's half of a K tile (64 keys x 128 cols as two 64x64 boxes), K-major
+// B operand.
+__device__ __forceinline__ uint64_t k_desc(uint32_t half_saddr, int kk) {
+  return sdesc(half_saddr + (kk >> 2) * KBOX_BYTES + (kk & 3) * 32, 16, 1024, SWZ_128B);
+}
+// This CTA's half of a V tile (128 keys x 64 head-dim columns, one box),
+// MN-major B operand of P.V; K-slice kk covers keys 16kk .. 16kk+15.
+__device__ __forceinline__ uint64_t v_desc(uint32_t half_saddr, int kk) {
+  return sdesc(half_saddr + kk * 16 * 128, HALF_BYTES, 1024, SWZ_128B);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK64,
+                const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const RingGeom& g = p.g;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < KSTAGE; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VSTAGE; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->s_full[q], 1);
+      mbar_init(&bars->p_full[q], 256);
+      mbar_init(&bars->o_full[q], 1);
+      mbar_init(&bars->o_empty[q], 256);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_base, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();          // both CTAs' barriers initialised before either touches the other's
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  clock_mark(p.clk, 0);
+  const WaitCtx wc{&bars->abort, p.status, WAIT_LIMIT_NS, cluster_ptr(&bars->abort, rank ^ 1u)};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK64);
+      tma_prefetch_desc(&tmV);
+      const uint32_t q_full0 = cluster_addr(&bars->q_full, 0);
+      uint32_t kv_it = 0, qe_ph = 0, nq = 0;
+      bool ok = true;
+      for (int64_t r = 0; ok; ++r) {
+        const int64_t u = snake_pos(r, cid, ncl);
+        if (u >= p.num_units) break;
+        const Unit w = unit_at(g, u);
+        if (nq > 0) {
+          if (!(ok = mbar_wait(&bars->q_empty, qe_ph, wc, ST_FWD_WAIT | 1))) break;
+          qe_ph ^= 1;
+        }
+        if (!(p.withhold_first_q && nq == 0)) {
+          if (leader) mbar_arrive_expect_tx(&bars->q_full, 4 * TILE_BYTES);
+          const int qrow = w.i * g.c + w.r0 + static_cast<int>(rank) * 2 * BM;
+          for (int q = 0; q < 2; ++q)
+            for (int h = 0; h < 2; ++h)
+              if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_Q, h * 64, qrow + q * BM, w.bh, HD, p.S + 3 * BM, p.BH, 8))
+                tma_load_3d_pair(smem + OFF_Q + q * TILE_BYTES + h * BOX_BYTES, &tmQ, q_full0, h * 64,
+                                 qrow + q * BM, w.bh);
+        }
+        ++nq;
+        for (int s = 0; s < g.N && ok; ++s) {
+          const int j = ring_block(w.i, s, g.N);
+          if (!block_visited(g, w.i, j)) continue;
+          const int last = kt_last(g, w.i, j, w.r0);
+          for (int kt = 0; kt <= last; ++kt) {
+            const int krow = j * g.c + kt * BN;
+            const int sk = kv_it % KSTAGE, sv = kv_it % VSTAGE;
+            if (!(ok = mbar_wait(&bars->k_empty[sk], ((kv_it / KSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 2))) break;
+            if (leader) mbar_arrive_expect_tx(&bars->k_full[sk], 2 * HALF_BYTES);
+            const uint32_t kf = cluster_addr(&bars->k_full[sk], 0);
+            const int krow_half = krow + static_cast<int>(rank) * 64;
+            for (int h = 0; h < 2; ++h)
+              if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_K, h * 64, krow_half, w.bh, HD, p.S + 64, p.BH, 8))
+                tma_load_3d_pair(smem + OFF_K + sk * HALF_BYTES + h * KBOX_BYTES, &tmK64, kf, h * 64, krow_half,
+                                 w.bh);
+            if (!(ok = mbar_wait(&bars->v_empty[sv], ((kv_it / VSTAGE) & 1) ^ 1, wc, ST_FWD_WAIT | 11))) break;
+            if (leader) mbar_arrive_expect_tx(&bars->v_full[sv], 2 * HALF_BYTES);
+            const int vx = static_cast<int>(rank) * 64;
+            if (RA_CHECK_BOX(p.chk, SITE_FWD_TMA_V, vx, krow, w.bh, HD, p.S, p.BH, 8))
+              tma_load_3d_pair(smem + OFF_V + sv * HALF_BYTES, &tmV, cluster_addr(&bars->v_full[sv], 0), vx, krow,
+                               w.bh);
+            ++kv_it;
+          }
+        }
+      }
+      if (!ok) {
+        // Copies in flight land within microseconds; hold the CTA (bounded) so
+        // none lands after it exits.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (leader) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(2 * BM, BN, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(2 * BM, HD, 0, 1);
+      uint32_t kv_it = 0, q_ph = 0, pf_ph[2] = {0, 0}, oe_ph[2] = {0, 0};
+      bool ok = true, first = true;
+      // Each barrier that both CTAs wait on is signalled with one commit per CTA.
+      auto commit_both = [](uint64_t* bar) {
+        mma_commit_pair_w(cluster_addr(bar, 0));
+        mma_commit_pair_w(cluster_addr(bar, 1));
+      };
+      auto issue_s = [=](int q, int st) {
+        const uint64_t dq0 = q_desc(sbase + OFF_Q + q * TILE_BYTES, 0);
+        const uint64_t dk0 = k_desc(sbase + OFF_K + st * HALF_BYTES, 0);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_pair_w(tmem + q * 128, sdesc_add(dq0, (kk >> 2) * BOX_BYTES + (kk & 3) * 32),
+                        sdesc_add(dk0, (kk >> 2) * KBOX_BYTES + (kk & 3) * 32), IDESC_QK, kk > 0);
+        commit_both(&bars->s_full[q]);
+      };
+      auto issue_pv = [=](int q, int st, uint32_t acc) {
+        const uint64_t dv0 = v_desc(sbase + OFF_V + st * HALF_BYTES, 0);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_pair_w(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, sdesc_add(dv0, kk * 16 * 128), IDESC_PV,
+                        (kk > 0) | acc);
+      };
+      for (int64_t r = 0; ok; ++r) {
+        const int64_t u = snake_pos(r, cid, ncl);
+        if (u >= p.num_units) break;
+        const Unit w = unit_at(g, u);
+        const int T = unit_tiles(g, w.i, w.r0);
+        if (!(ok = mbar_wait_w(&bars->q_full, q_ph, wc, ST_FWD_WAIT | 3))) break;
+        q_ph ^= 1;
+        {
+          const int sk = kv_it % KSTAGE;
+          if (!(ok = mbar_wait_w(&bars->k_full[sk], (kv_it / KSTAGE) & 1, wc, ST_FWD_WAIT | 4))) break;
+          tc_fence_after();
+          issue_s(0, sk);
+          issue_s(1, sk);
+          commit_both(&bars->k_empty[sk]);
+        }
+        for (int t = 0; t < T && ok; ++t, ++kv_it) {
+          const int sv = kv_it % VSTAGE;
+          const int nsk = (kv_it + 1) % KSTAGE;
+          const uint32_t nph = ((kv_it + 1) / KSTAGE) & 1;
+          if (!(ok = mbar_wait_w(&bars->v_full[sv], (kv_it / VSTAGE) & 1, wc, ST_FWD_WAIT | 5))) break;
+          for (int q = 0; q < 2 && ok; ++q) {
+            if (t == 0 && !first) {
+              if (!(ok = mbar_wait_w(&bars->o_empty[q], oe_ph[q], wc, ST_FWD_WAIT | 6))) break;
+              oe_ph[q] ^= 1;
+            }
+            if (!(ok = mbar_wait_w(&bars->p_full[q], pf_ph[q], wc, ST_FWD_WAIT | 7))) break;
+            pf_ph[q] ^= 1;
+            tc_fence_after();
+            issue_pv(q, sv, t > 0 ? 1u : 0u);
+            if (q == 1) commit_both(&bars->v_empty[sv]);
+            if (t == T - 1) {
+              if (q == 0) commit_both(&bars->q_empty);
+              commit_both(&bars->o_full[q]);
+            } else {
+              if (q == 0) {
+                if (!(ok = mbar_wait_w(&bars->k_full[nsk], nph, wc, ST_FWD_WAIT | 8))) break;
+                tc_fence_after();
+              }
+              issue_s(q, nsk);
+              if (q == 1) commit_both(&bars->k_empty[nsk]);
+            }
+          }
+        }
+        first = false;
+      }
+      // Every MMA of the pair has finished before either CTA frees TMEM.
+      mma_commit_pair_w(cluster_addr(&bars->drain, 0));
+      mbar_drain(&bars->drain, 0, 200000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (both CTAs)
+    const int q = (warp - 2) >> 2;         // Q tile 0 or 1
+    const int quad = warp & 3;             // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;      // row inside the Q tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + q * 128;
+    const uint32_t tO = tmem + lane_off + 256 + q * 128;
+    const uint32_t p_full0 = cluster_addr(&bars->p_full[q], 0);
+    const uint32_t o_empty0 = cluster_addr(&bars->o_empty[q], 0);
+    const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
+    const bool timer = p.timing && leader && warp == 2 && lane == 0;
+    uint32_t s_ph = 0, o_ph = 0;
+    bool ok = true;
+    for (int64_t r = 0; ok; ++r) {
+      const int64_t u = snake_pos(r, cid, ncl);
+      if (u >= p.num_units) break;
+      const Unit w = unit_at(g, u);
+      const int rq = w.r0 + static_cast<int>(rank) * 2 * BM + q * BM + row;  // row inside query block i
+      float fold_lse_a = -INFINITY;        // fold mode: the state row's LSE, read while the unit runs
+      if (p.O_acc && rq < g.c) {           // and its O row brought into L2 for the unit's end
+        const int64_t gi = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
+        const char* srow = reinterpret_cast<const char*>(p.O_acc + gi * HD);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + 128 * k));
+        if (RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, gi, 1, p.BH * p.S)) fold_lse_a = p.LSE_acc[gi];
+      }
+      float m_use = -INFINITY, l = 0.f;
+      int t = 0, s_prev = -1;
+      uint64_t t_step0 = 0;
+      for (int s = 0; s < g.N && ok; ++s) {
+        const int j = ring_block(w.i, s, g.N);
+        if (!block_visited(g, w.i, j)) continue;
+        const int last = kt_last(g, w.i, j, w.r0);
+        const int lim = key_limit(g, w.i, j, rq);
+        for (int kt = 0; kt <= last; ++kt, ++t) {
+          if (!(ok = mbar_wait(&bars->s_full[q], s_ph, wc, ST_FWD_WAIT | 9))) break;
+          s_ph ^= 1;
+          tc_fence_after();
+          if (timer && kt == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (s_prev >= 0) atomicAdd(&p.timing[w.i * g.N + s_prev], now - t_step0);
+            s_prev = s;
+            t_step0 = now;
+          }
+          float sv[BN];
+          uint32_t* su = reinterpret_cast<uint32_t*>(sv);
+          tmem_ld32(tS + 0, su);
+          tmem_ld32(tS + 32, su + 32);
+          tmem_ld32(tS + 64, su + 64);
+          tmem_ld32(tS + 96, su + 96);
+          tmem_ld_wait();
+          if (tile_masked(g, w.i, j, kt, w.r0)) {
+            const int rk0 = kt * BN;
+#pragma unroll
+            for (int k = 0; k < BN; ++k)
+              if (rk0 + k >= lim) sv[k] = -INFINITY;
+          }
+          float mx0 = fmaxf(sv[0], sv[4]), mx1 = fmaxf(sv[1], sv[5]), mx2 = fmaxf(sv[2], sv[6]),
+                mx3 = fmaxf(sv[3], sv[7]);
+#pragma unroll
+          for (int k = 8; k < BN; k += 8) {
+            mx0 = fmax3(mx0, sv[k], sv[k + 4]);
+            mx1 = fmax3(mx1, sv[k + 1], sv[k + 5]);
+            mx2 = fmax3(mx2, sv[k + 2], sv[k + 6]);
+            mx3 = fmax3(mx3, sv[k + 3], sv[k + 7]);
+          }
+          const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+          // Rescale only when the max grew by more than the threshold: O and
+          // l then share a stale reference max, which cancels in O / l.
+          const float mt = mx * sl2;
+          const bool grow = mt > m_use + RESCALE_THRESHOLD;
+          float alpha = 1.f;
+          if (grow) {
+            alpha = hw_exp2(m_use - mt);   // 0 when nothing was seen before
+            l *= alpha;
+            m_use = mt;
+          }
+          const bool rescale_o = (t > 0) && __any_sync(0xffffffffu, grow);
+#if RA_CHECKS
+          if (rescale_o && grow) RA_COUNT(p.chk, EV_FWD_RESCALE_ROWS, 1);
+          if (rescale_o && lane == 0) RA_COUNT(p.chk, EV_FWD_RESCALE_WARPS, 1);
+#endif
+          const float mref = (m_use == -INFINITY) ? 0.f : m_use;
+          const float2 nm2 = make_float2(-mref, -mref);
+          float2 rs2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 a = __ffma2_rn(make_float2(sv[ch * 32 + k], sv[ch * 32 + k + 1]), sl2v, nm2);
+              const float2 pp = make_float2(hw_exp2(a.x), hw_exp2(a.y));
+              rs2 = __fadd2_rn(rs2, pp);
+              pk[k >> 1] = pack_bf16x2(pp.x, pp.y);
+            }
+            tmem_st16(tS + ch * 16, pk);
+          }
+          l += rs2.x + rs2.y;
+          if (rescale_o) {   // O_q is idle: PV_q(t-1) completed before S_q(t) was signalled
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              uint32_t ov[32];
+              tmem_ld32(tO + ch * 32, ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ov[k]), __uint_as_float(ov[k + 1])),
+                                             make_float2(alpha, alpha));
+                ov[k] = __float_as_uint(o2.x);
+                ov[k + 1] = __float_as_uint(o2.y);
+              }
+              tmem_st32(tO + ch * 32, ov);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_cl(p_full0);
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+      if (!(ok = mbar_wait(&bars->o_full[q], o_ph, wc, ST_FWD_WAIT | 10))) break;
+      o_ph ^= 1;
+      tc_fence_after();
+      if (timer && s_prev >= 0) atomicAdd(&p.timing[w.i * g.N + s_prev], globaltimer_ns() - t_step0);
+      bool valid = rq < g.c;
+      const int64_t grow_idx = static_cast<int64_t>(w.bh) * p.S + static_cast<int64_t>(w.i) * g.c + rq;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      if (p.O_acc) {
+        // Fold mode: LogSumExp-merge this call's partial (O = acc / l, lse_b) into the row of the
+        // running float32 state, which this thread alone owns.  A state row with LSE -inf is
+        // empty and is not read; a partial with no visible key leaves the row as it is.
+        if (valid && !(RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, grow_idx * HD, HD, p.BH * p.S * HD) &&
+                       RA_CHECK_RANGE(p.chk, SITE_FWD_FOLD, grow_idx, 1, p.BH * p.S)))
+          valid = false;
+        const float lse_b = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
+        const float lse_a = valid ? fold_lse_a : -INFINITY;
+        const bool fold = valid && lse_b != -INFINITY;
+        float wa = 0.f, wb = 0.f, lse_n = lse_a;
+        if (fold) {
+          const float M = fmaxf(lse_a, lse_b);
+          const float ea = expf(lse_a - M), eb = expf(lse_b - M);
+          lse_n = M + logf(ea + eb);
+          wa = ea / (ea + eb);
+          wb = eb / (ea + eb) * inv_l;   // the partial's O is acc * inv_l
+        }
+        float4* srow4 = reinterpret_cast<float4*>(p.O_acc + grow_idx * HD);
+        const bool read_a = fold && lse_a != -INFINITY;
+        float4 st[2][8];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) st[0][v4] = read_a ? srow4[v4] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch + 1 < 4) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              st[(ch + 1) & 1][v4] = read_a ? srow4[(ch + 1) * 8 + v4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          uint32_t ov[32];
+          tmem_ld32(tO + ch * 32, ov);
+          tmem_ld_wait();
+          if (fold) {
+            float4* dst = srow4 + ch * 8;
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 a = st[ch & 1][v4];
+              a.x = fmaf(wb, __uint_as_float(ov[4 * v4]), wa * a.x);
+              a.y = fmaf(wb, __uint_as_float(ov[4 * v4 + 1]), wa * a.y);
+              a.z = fmaf(wb, __uint_as_float(ov[4 * v4 + 2]), wa * a.z);
+              a.w = fmaf(wb, __uint_as_float(ov[4 * v4 + 3]), wa * a.w);
+              dst[v4] = a;
+            }
+          }
+        }
+        if (fold) p.LSE_acc[grow_idx] = lse_n;
+        tc_fence_before();
+        mbar_arrive_cl(o_empty0);
+        continue;
+      }
+      __nv_bfloat16* orow = p.O + grow_idx * HD;
+      if (valid && !RA_CHECK_RANGE(p.chk, SITE_FWD_O, grow_idx * HD, HD, p.BH * p.S * HD)) valid = false;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t ov[32];
+        tmem_ld32(tO + ch * 32, ov);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv_l, __uint_as_float(ov[2 * k + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (valid && RA_CHECK_RANGE(p.chk, SITE_FWD_LSE, grow_idx, 1, p.BH * p.S))
+        p.LSE[grow_idx] = l > 0.f ? (m_use + hw_log2(l)) * 0.6931471805599453f : -INFINITY;
+      tc_fence_before();
+      mbar_arrive_cl(o_empty0);
+    }
+  }
+
+  // Both CTAs are done with TMEM (rank 0 drained every MMA; the softmax warps
+  // of both have finished their loads) and neither will touch the other's
+  // shared memory again.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  clock_mark(p.clk, 1);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+}  // namespace fwdp
+
+int fwd_pair_clusters() {
+  static std::atomic<int> cached[64];   // per device: 0 = not yet asked, else slots + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  const int c = cached[dev].load();
+  if (c > 0) return c - 1;
+  if (raise_smem_limit(reinterpret_cast<const void*>(fwdp::fwd_pair_kernel), fwdp::SMEM_BYTES) != cudaSuccess)
+    return -1;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  cfg.blockDim = dim3(fwdp::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = fwdp::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fwdp::fwd_pair_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  cached[dev].store(n + 1);
+  return n;
+}
+
+cudaError_t launch_fwd_bf16_pair(const FwdArgs& a, const void* tmap_q, const void* tmap_k64, const void* tmap_v) {
+  using namespace fwdp;
+  Params p;
+  p.g.N = static_cast<int>(a.N);
+  p.g.c = static_cast<int>(a.S / a.N);
+  p.g.causal = a.causal;
+  p.g.striped = a.striped;
+  p.g.strict = a.strict;
+  p.g.kt_w = BN;
+  p.g.n_kt = (p.g.c + BN - 1) / BN;
+  p.g.mb_h = UNIT_ROWS;
+  p.g.n_mb = (p.g.c + UNIT_ROWS - 1) / UNIT_ROWS;
+  p.S = static_cast<int>(a.S);
+  p.num_units = a.B * a.H * a.N * p.g.n_mb;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
+  p.O = static_cast<__nv_bfloat16*>(a.O);
+  p.LSE = a.LSE;
+  p.status = a.status;
+  p.timing = a.timing;
+  p.withhold_first_q = a.withhold_first_q;
+  p.BH = a.B * a.H;
+  p.chk = a.chk;
+  p.O_acc = a.O_acc;
+  p.LSE_acc = a.LSE_acc;
+  p.clk = a.clk;
+  const int max_cl = fwd_pair_clusters();   // also raises the kernel's shared-memory limit
+  if (max_cl < 1) return cudaErrorInvalidConfiguration;
+  const int64_t ncl64 = p.num_units < max_cl ? p.num_units : max_cl;
+  const int ncl = static_cast<int>(ncl64 > 0 ? ncl64 : 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.ev) cudaEventRecord(a.ev[0], a.stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fwd_pair_kernel, *static_cast<const CUtensorMap*>(tmap_q),
+                                     *static_cast<const CUtensorMap*>(tmap_k64),
+                                     *static_cast<const CUtensorMap*>(tmap_v), p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (a.ev) cudaEventRecord(a.ev[1], a.stream);
+  return e;
+}
+
+}  // namespace ra

@@ -42,6 +42,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 // ---------------------------------------------------------------- device state
 __device__ unsigned int g_device_status;  // first bounded-wait time-out code, 0 if none
 __device__ ra::CheckRec g_check_rec;      // bounds checks and event counts (checked build)
+// SM clock records of timed kernels: block 0's clock64 and %globaltimer at its
+// start and at its end (a ring of slots handed out by kt_begin).
+constexpr int kClkSlots = 256;
+__device__ unsigned long long g_clk_rec[kClkSlots][4];
 
 constexpr int kMaxDevices = 64;
 struct DevState {
@@ -49,6 +53,7 @@ struct DevState {
   int num_sms = 0;
   unsigned int* status = nullptr;  // device address of g_device_status
   ra::CheckRec* chk = nullptr;     // device address of g_check_rec
+  unsigned long long* clk = nullptr;   // device address of g_clk_rec
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -75,6 +80,9 @@ int device_state(DevState** out) {
     e = cudaGetSymbolAddress(&p, g_check_rec);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(check record)");
     d.chk = static_cast<ra::CheckRec*>(p);
+    e = cudaGetSymbolAddress(&p, g_clk_rec);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(clock records)");
+    d.clk = static_cast<unsigned long long*>(p);
     d.ready = true;
   }
   *out = &d;
@@ -82,6 +90,7 @@ int device_state(DevState** out) {
 }
 
 std::atomic<int> g_wait_test{0};   // one-shot: next bf16 forward withholds its first Q tile
+std::atomic<int> g_fwd_kernel{RA_FWD_SINGLE};   // which bf16 forward kernel (ra_set_fwd_kernel)
 std::atomic<uint64_t*> g_timing_buf{nullptr};
 std::atomic<size_t> g_timing_n{0};
 
@@ -94,20 +103,32 @@ struct TimedCall {
   int nk;             // kernels timed (events = nk + 1)
   int dev;
   cudaEvent_t ev[kMaxTimedKernels + 1];
+  int k0;             // kernel index of the first timed kernel
+  int slot[kMaxTimedKernels];   // clock record slot of each kernel, or -1
 };
 std::atomic<bool> g_kt_on{false};
 std::mutex g_kt_mu;
 std::deque<TimedCall> g_kt_calls;
 std::map<int, std::vector<cudaEvent_t>> g_kt_pool;   // idle events per device
+int g_clk_next = 0, g_clk_used = 0;                  // clock slots (guarded by g_kt_mu)
 
-// Events for one call of `nk` kernels on the current device, or null when
-// timing is off (or an event cannot be created: the call then runs untimed).
-cudaEvent_t* kt_begin(int call, int nk) {
+// Events (and clock record slots for the kernels in `clock_mask`) for one call
+// of `nk` kernels on the current device, or null when timing is off (or an
+// event cannot be created: the call then runs untimed).
+TimedCall* kt_begin(int call, int nk, int k0 = 0, unsigned clock_mask = 0) {
   if (!g_kt_on.load() || nk > kMaxTimedKernels) return nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lk(g_kt_mu);
-  TimedCall tc{call, nk, dev, {}};
+  TimedCall tc{call, nk, dev, {}, k0, {}};
+  for (int k = 0; k < nk; ++k) {
+    tc.slot[k] = -1;
+    if ((clock_mask >> k) & 1u && g_clk_used < kClkSlots) {
+      tc.slot[k] = g_clk_next;
+      g_clk_next = (g_clk_next + 1) % kClkSlots;
+      ++g_clk_used;
+    }
+  }
   auto& pool = g_kt_pool[dev];
   for (int k = 0; k <= nk; ++k) {
     if (pool.empty()) {
@@ -122,7 +143,12 @@ cudaEvent_t* kt_begin(int call, int nk) {
     pool.pop_back();
   }
   g_kt_calls.push_back(tc);
-  return g_kt_calls.back().ev;
+  return &g_kt_calls.back();
+}
+cudaEvent_t* kt_events(TimedCall* tc) { return tc ? tc->ev : nullptr; }
+// The clock record of kernel k of a timed call, or null.
+unsigned long long* kt_clock(const DevState* d, const TimedCall* tc, int k) {
+  return (tc && tc->slot[k] >= 0) ? d->clk + 4 * static_cast<size_t>(tc->slot[k]) : nullptr;
 }
 
 // ---------------------------------------------------------------- TMA maps
@@ -219,7 +245,16 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
   a.timing = reinterpret_cast<unsigned long long*>(timing);
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
-  a.ev = kt_begin(RA_CALL_FWD, 1);
+  // bf16: the SM-pair kernel (2-CTA clusters) when selected, else one CTA per SM.
+  const bool pair = dtype == RA_BF16 && g_fwd_kernel.load() == RA_FWD_PAIR;
+  if (pair) {
+    const int slots = ra::fwd_pair_clusters();
+    if (slots < 0) return fail(RA_ERR_CUDA, "ra_fwd: cluster occupancy query failed");
+    if (slots == 0) return fail(RA_ERR_UNSUPPORTED, "ra_fwd: no 2-CTA cluster of the pair kernel fits on this device");
+  }
+  TimedCall* tc = kt_begin(RA_CALL_FWD, 1, pair ? 1 : 0, dtype == RA_BF16 ? 1u : 0u);
+  a.ev = kt_events(tc);
+  a.clk = kt_clock(d, tc, 0);
   a.chk = d->chk;
   a.O_acc = O_acc;
   a.LSE_acc = LSE_acc;
@@ -227,9 +262,9 @@ int fwd_impl(const void* Q, const void* K, const void* V, int64_t B, int64_t H, 
   if (dtype == RA_BF16) {
     CUtensorMap mq, mk, mv;
     if ((rc = make_map_bf16(&mq, Q, B * H, S, D, 128)) != RA_OK) return rc;
-    if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
+    if ((rc = make_map_bf16(&mk, K, B * H, S, D, pair ? 64 : 128)) != RA_OK) return rc;
     if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
-    e = ra::launch_fwd_bf16(a, &mq, &mk, &mv);
+    e = pair ? ra::launch_fwd_bf16_pair(a, &mq, &mk, &mv) : ra::launch_fwd_bf16(a, &mq, &mk, &mv);
   } else {
     e = ra::launch_fwd_f32(a);
   }
@@ -294,6 +329,13 @@ int ra_set_wait_test(int enable) {
   return RA_OK;
 }
 
+int ra_set_fwd_kernel(int kind) {
+  if (kind != RA_FWD_SINGLE && kind != RA_FWD_PAIR)
+    return fail(RA_ERR_ARG, "ra_set_fwd_kernel: kind must be RA_FWD_SINGLE or RA_FWD_PAIR (got %d)", kind);
+  g_fwd_kernel.store(kind);
+  return RA_OK;
+}
+
 int ra_set_kernel_timing(int enable) {
   if (enable != 0 && enable != 1) return fail(RA_ERR_ARG, "ra_set_kernel_timing: enable must be 0 or 1");
   std::lock_guard<std::mutex> lk(g_kt_mu);
@@ -302,6 +344,7 @@ int ra_set_kernel_timing(int enable) {
     for (auto& c : g_kt_calls)
       for (int k = 0; k <= c.nk; ++k) g_kt_pool[c.dev].push_back(c.ev[k]);
     g_kt_calls.clear();
+    g_clk_used = 0;
   }
   return RA_OK;
 }
@@ -316,9 +359,15 @@ int ra_kernel_times(ra_kernel_time* out, int capacity, int* count) {
     if (prev != c.dev) cudaSetDevice(c.dev);
     cudaError_t e = cudaEventSynchronize(c.ev[c.nk]);
     for (int k = 0; k < c.nk; ++k) {
-      float ms = -1.f;
+      float ms = -1.f, mhz = -1.f;
       if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, c.ev[k], c.ev[k + 1]);
-      if (n < capacity) out[n] = ra_kernel_time{c.call, k, ms};
+      if (e == cudaSuccess && c.slot[k] >= 0) {
+        unsigned long long r[4] = {0, 0, 0, 0};
+        e = cudaMemcpyFromSymbol(r, g_clk_rec, sizeof(r), sizeof(r) * static_cast<size_t>(c.slot[k]));
+        if (e == cudaSuccess && r[3] > r[1] && r[2] > r[0])
+          mhz = static_cast<float>(static_cast<double>(r[2] - r[0]) / static_cast<double>(r[3] - r[1]) * 1e3);
+      }
+      if (n < capacity) out[n] = ra_kernel_time{c.call, c.k0 + k, ms, mhz};
       ++n;
     }
     if (prev != c.dev) cudaSetDevice(prev);
@@ -326,6 +375,7 @@ int ra_kernel_times(ra_kernel_time* out, int capacity, int* count) {
     for (int k = 0; k <= c.nk; ++k) g_kt_pool[c.dev].push_back(c.ev[k]);
   }
   g_kt_calls.clear();
+  g_clk_used = 0;
   *count = n;
   if (rc == RA_OK && n > capacity)
     rc = fail(RA_ERR_ARG, "ra_kernel_times: %d records, room for %d (the rest were dropped)", n, capacity);
@@ -509,7 +559,10 @@ int bwd_impl(const char* who, const void* Q, const void* K, const void* V, const
   if ((rc = make_map_bf16(&mk, K, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mv, V, B * H, S, D, 128)) != RA_OK) return rc;
   if ((rc = make_map_bf16(&mdo, dO, B * H, S, D, 128)) != RA_OK) return rc;
-  a.ev = accumulate ? nullptr : kt_begin(RA_CALL_BWD, 3);
+  TimedCall* tc = accumulate ? nullptr : kt_begin(RA_CALL_BWD, 3, 0, 0x6u);
+  a.ev = kt_events(tc);
+  a.clk_dkv = kt_clock(d, tc, 1);
+  a.clk_dq = kt_clock(d, tc, 2);
   cudaError_t e = ra::launch_bwd_bf16(a, &mq, &mk, &mv, &mdo);
   if (e == cudaErrorNotSupported) return fail(RA_ERR_UNSUPPORTED, "%s: kernel not built", who);
   if (e != cudaSuccess) return cuda_fail(e, who);
@@ -607,7 +660,7 @@ int ra_decode(const void* q, const void* K, const void* V, int64_t B, int64_t H,
   a.status = d->status;
   a.stream = static_cast<cudaStream_t>(stream);
   a.num_sms = d->num_sms;
-  a.ev = kt_begin(RA_CALL_DECODE, 2);
+  a.ev = kt_events(kt_begin(RA_CALL_DECODE, 2));
   a.chk = d->chk;
   cudaError_t e = ra::launch_decode_bf16(a);
   if (e != cudaSuccess) return cuda_fail(e, "ra_decode launch");
@@ -664,7 +717,7 @@ int ra_ffn(const void* X, const void* W1, const void* W3, const void* W2, void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t me = cudaMemsetAsync(counters, 0, static_cast<size_t>(2 * nblocks) * sizeof(int), st);
   if (me != cudaSuccess) return cuda_fail(me, "ra_ffn: clearing the tile counters");
-  cudaEvent_t* ev = kt_begin(RA_CALL_FFN, static_cast<int>(2 * nblocks));
+  cudaEvent_t* ev = kt_events(kt_begin(RA_CALL_FFN, static_cast<int>(2 * nblocks)));
   for (int64_t b = 0; b < nblocks; ++b) {
     const int64_t r0 = b * c, rows = (T - r0 < c) ? T - r0 : c;
     const char* xb = static_cast<const char*>(X) + r0 * h * 2;

@@ -18,6 +18,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Clock record of a timed kernel: block 0's thread 0 writes (clock64,
+// %globaltimer) into rec[0..1] when it starts and rec[2..3] when it ends, so
+// the host can tell the SM clock the kernel ran at.
+__device__ __forceinline__ void clock_mark(unsigned long long* rec, int at_end) {
+  if (rec && blockIdx.x == 0 && threadIdx.x == 0) {
+    rec[2 * at_end] = static_cast<unsigned long long>(clock64());
+    rec[2 * at_end + 1] = globaltimer_ns();
+  }
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -52,6 +62,7 @@ struct WaitCtx {
   volatile int* abort;      // shared-memory flag of this CTA
   unsigned int* status;     // device status word (first failure wins)
   uint64_t limit_ns;
+  volatile int* peer_abort = nullptr;  // CTA pairs: the other CTA's flag (distributed shared memory)
 };
 
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w,
@@ -62,6 +73,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     if (*w.abort) return false;
     if ((it & 63u) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
       *w.abort = 1;
+      if (w.peer_abort) *w.peer_abort = 1;
       atomicCAS(w.status, 0u, where);
       return false;
     }
@@ -279,6 +291,101 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ------------------------------------------------- CTA pairs (cluster of 2)
+// Thread-block cluster of two CTAs on an SM pair: rank 0 issues the pair's
+// tcgen05 MMAs (cta_group::2), whose M = 256 rows are 128 rows of A from each
+// CTA's shared memory or TMEM, whose B operand is split in half along N
+// between the two CTAs (same shared-memory offset in each), and whose result
+// lands in each CTA's own TMEM (its 128 rows).  All tcgen05 instructions of
+// such a kernel use cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the object at `local` in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  return a;
+}
+// Generic pointer to the object at `local` in the CTA of rank `rank`.
+template <typename T>
+__device__ __forceinline__ T* cluster_ptr(T* local, uint32_t rank) {
+  uint64_t a;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(a) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<T*>(a);
+}
+// Every thread of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Arrive on a barrier given by its shared::cluster address (either CTA of the
+// pair), with the instruction's default release semantics at CTA scope.  The
+// pair kernels publish only TMEM state the arriving thread has already waited
+// for (tcgen05.wait::st / wait::ld, then tcgen05.fence::before_thread_sync);
+// a release at cluster scope costs about a thousand cycles an arrival here and
+// made the pair forward 37 % slower.
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+// 3-D tiled load into this CTA's shared memory whose byte count completes on a
+// barrier of either CTA of the pair (`bar_cl`, a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cl,
+                                                 int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// TMEM allocation for a pair: one warp of each CTA runs these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Warp-wide pair MMAs and commit (one elected lane issues, as above).
+__device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// Arrive once on the barrier at `bar_cl` (either CTA of the pair) when every
+// pair MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair_w(uint32_t bar_cl) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar_cl));
 }
 
 }  // namespace ra

@@ -16,3 +16,13 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(params=["single", "pair"])
+def fwd_kernel(request):
+    """Runs a bf16 forward test once with each forward kernel (one CTA per SM,
+    and SM pairs); the choice is process-wide, so it is reset afterwards."""
+    import ring_attention_fwd_gb300 as ra
+    ra.set_fwd_kernel(request.param)
+    yield request.param
+    ra.set_fwd_kernel("single")

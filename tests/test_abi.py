@@ -35,7 +35,7 @@ def test_header_declares_the_api():
     assert declared_symbols() == sorted([
         "ra_fwd", "ra_fwd_step", "ra_fwd_step_fold", "ra_merge", "ra_bwd_workspace_bytes", "ra_bwd", "ra_bwd_step", "ra_bwd_noalloc",
         "ra_decode_workspace_bytes", "ra_decode", "ra_ffn_workspace_bytes", "ra_ffn", "ra_set_timing_buffer",
-        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_check_device_status",
+        "ra_set_kernel_timing", "ra_kernel_times", "ra_set_wait_test", "ra_set_fwd_kernel", "ra_check_device_status",
         "ra_read_checks", "ra_last_error", "ra_version"])
 
 
@@ -231,6 +231,16 @@ def test_ffn_workspace_and_bad_arguments(L):
 def test_wait_test_switch_arguments(L):
     assert L.ra_set_wait_test(3) == 1
     assert L.ra_set_wait_test(0) == 0
+
+
+def test_fwd_kernel_switch_arguments(L):
+    from ring_attention_fwd_gb300 import binding
+    assert L.ra_set_fwd_kernel(2) == 1 and "RA_FWD_PAIR" in L.ra_last_error().decode()
+    assert L.ra_set_fwd_kernel(-1) == 1
+    for kind in (1, 0):                    # ends on the default
+        assert L.ra_set_fwd_kernel(kind) == 0
+    with pytest.raises(ValueError):
+        binding.set_fwd_kernel("dual")
 
 
 def test_kernel_timing_arguments(L):

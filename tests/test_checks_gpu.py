@@ -57,7 +57,7 @@ def _grad_close(g, ref, name):
     (3, 2, 768, 3, True, "striped"),        # B > 1
     (2, 1, 1024, 4, False, "contiguous"),
 ])
-def test_checked_forward_backward(ra, B, H, S, N, causal, layout):
+def test_checked_forward_backward(ra, fwd_kernel, B, H, S, N, causal, layout):
     inp = make_inputs(B, H, S, 128, seed=700 + S + N, with_grad=True)
     q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
     dev = {x: inp[x].cuda() for x in ("q", "k", "v", "do")}
@@ -154,7 +154,7 @@ def test_checked_feedforward(ra):
 
 
 @pytest.mark.parametrize("B,H,S,N,causal,layout,mode", PEAKED_CASES)
-def test_checked_counts_forced_rescales(ra, B, H, S, N, causal, layout, mode):
+def test_checked_counts_forced_rescales(ra, fwd_kernel, B, H, S, N, causal, layout, mode):
     """Device count of rows whose O was rescaled >= what the inputs force."""
     inp = make_peaked_inputs(B, H, S, N, seed=500 + S + N, mode=mode)
     q, k = as_float64(inp["q"]), as_float64(inp["k"])

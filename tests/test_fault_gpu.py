@@ -12,7 +12,7 @@ from ring_attention_fwd_gb300.inputs import make_inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_tile_times_out_cleanly_and_device_stays_usable():
+def test_withheld_tile_times_out_cleanly_and_device_stays_usable(fwd_kernel):
     import ring_attention_fwd_gb300 as ra
     L = ra.binding.lib()
     inp = {k: v.cuda() for k, v in make_inputs(1, 2, 1024, 128, seed=41).items()}

@@ -35,7 +35,7 @@ def _attn_cases(n, seed):
 
 @pytest.mark.parametrize("case", _attn_cases(12, 2024), ids=lambda c: f"B{c['B']}H{c['H']}S{c['S']}N{c['N']}"
                          f"{'c' if c['causal'] else 'n'}{c['layout'][0]}")
-def test_fuzz_forward_backward(ra, case):
+def test_fuzz_forward_backward(ra, fwd_kernel, case):
     B, H, S, N = case["B"], case["H"], case["S"], case["N"]
     inp = make_inputs(B, H, S, 128, seed=case["seed"], with_grad=True)
     dev = {k: v.cuda() for k, v in inp.items()}

@@ -52,7 +52,7 @@ BF16_CASES = [
 
 
 @pytest.mark.parametrize("B,H,S,N,causal,layout", BF16_CASES)
-def test_bf16_shapes(ra, B, H, S, N, causal, layout):
+def test_bf16_shapes(ra, fwd_kernel, B, H, S, N, causal, layout):
     inp = make_inputs(B, H, S, 128, seed=200 + S + N, dtype="bf16")
     eo, el = fwd_full_check(ra, inp, N, causal, layout, "bf16")
     assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
@@ -128,7 +128,7 @@ def test_fwdbwd_64k_workload_forward_every_head(ra):
     assert eo <= TOL["bf16"]["o"] and el <= TOL["bf16"]["lse"], (eo, el)
 
 
-def test_per_device_timing_buffer(ra):
+def test_per_device_timing_buffer(ra, fwd_kernel):
     """Timing hooks: every visited (virtual host, ring step) gets time, every
     skipped one (contiguous causal, j > i) none."""
     N = 4
@@ -147,6 +147,55 @@ def test_per_device_timing_buffer(ra):
             assert (t[i, s] > 0) == (j <= i), (i, s, t)
 
 
+PAIR_EQUAL_CASES = [
+    (1, 2, 1024, 2, True, "contiguous", 1.0),
+    (1, 3, 4000, 4, True, "striped", 1.0),      # c = 1000: ragged units and KV tiles
+    (2, 2, 2000, 2, False, "contiguous", 1.0),
+    (1, 2, 200, 4, True, "contiguous", 1.0),     # c = 50: a pair unit holds all of a block
+    (1, 4, 32768, 8, True, "contiguous", 4.0),   # peaked scores: O rescaled mid-sweep
+    (1, 32, 131072, 32, True, "contiguous", 0.5),  # the 131072-token workload's shape
+]
+
+
+@pytest.mark.parametrize("B,H,S,N,causal,layout,scale", PAIR_EQUAL_CASES)
+def test_pair_and_single_kernels_bit_identical(ra, B, H, S, N, causal, layout, scale):
+    """The SM-pair forward issues the same MMAs over the same tiles, in the
+    same order, and runs the same per-row softmax code as the one-CTA-per-SM
+    kernel: O and LSE agree bit for bit, including rows beyond a ragged block
+    and rows that rescale."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(S + N)
+    q, k, v = (torch.randn((B, H, S, 128), device="cuda", generator=g).mul_(scale).to(torch.bfloat16)
+               for _ in range(3))
+    out = {}
+    try:
+        for kind in ("single", "pair"):
+            ra.set_fwd_kernel(kind)
+            out[kind] = ra.fwd(q, k, v, N, causal, layout)
+            torch.cuda.synchronize()
+            ra.check_device_status()
+    finally:
+        ra.set_fwd_kernel("single")
+    assert torch.equal(out["single"][0], out["pair"][0])
+    assert torch.equal(out["single"][1], out["pair"][1])
+
+
+def test_kernel_selection_and_names(ra):
+    """The timing records name the forward kernel that ran."""
+    inp = {x: torch.randn((1, 2, 1024, 128), device="cuda").to(torch.bfloat16) for x in "qkv"}
+    names = []
+    for kind in ("pair", "single"):
+        ra.set_fwd_kernel(kind)
+        ra.set_kernel_timing(True)
+        try:
+            ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "contiguous")
+            names.append([n for n, _ in ra.kernel_times()])
+        finally:
+            ra.set_kernel_timing(False)
+            ra.set_fwd_kernel("single")
+    assert names == [["fwd_pair"], ["fwd"]]
+
+
 def test_kernel_timing_records(ra):
     """Opt-in kernel timing: one record per kernel of every timed call, in
     order, with positive durations; nothing is recorded once it is off."""
@@ -155,10 +204,14 @@ def test_kernel_timing_records(ra):
     try:
         o, lse = ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
         ra.bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], 4, True, "striped")
-        t = ra.kernel_times()
+        t = ra.kernel_times(with_clock=True)
     finally:
         ra.set_kernel_timing(False)
-    assert [n for n, _ in t] == ["fwd", "bwd_prep", "bwd_dkv", "bwd_dq"]
-    assert all(ms > 0 for _, ms in t)
+    assert [n for n, _, _ in t] == ["fwd", "bwd_prep", "bwd_dkv", "bwd_dq"]
+    assert all(ms > 0 for _, ms, _ in t)
+    mhz = {n: c for n, _, c in t}
+    assert mhz["bwd_prep"] == -1                       # no clock record for the preprocess
+    for n in ("fwd", "bwd_dkv", "bwd_dq"):             # the tensor-core kernels report their SM clock
+        assert 200 < mhz[n] < 2600, (n, mhz[n])
     ra.fwd(inp["q"], inp["k"], inp["v"], 4, True, "striped")
     assert ra.kernel_times() == []

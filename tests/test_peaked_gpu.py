@@ -72,7 +72,7 @@ def _close(g, ref, floor, name, margin=1.25):
 
 
 @pytest.mark.parametrize("B,H,S,N,causal,layout,mode", PEAKED_CASES)
-def test_peaked_forward_backward(ra, B, H, S, N, causal, layout, mode):
+def test_peaked_forward_backward(ra, fwd_kernel, B, H, S, N, causal, layout, mode):
     inp = make_peaked_inputs(B, H, S, N, seed=500 + S + N, mode=mode)
     q, k, v, do = (as_float64(inp[x]) for x in ("q", "k", "v", "do"))
     ro, rl = orc.naive_attention(q, k, v, N, causal, layout)

@@ -26,7 +26,7 @@ def _blocks(t, N):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("layout", ["contiguous", "striped"])
-def test_single_pairs_match_oracle(ra, layout, dtype):
+def test_single_pairs_match_oracle(ra, fwd_kernel, layout, dtype):
     N, c = 4, 200 if dtype == "bf16" else 48
     D = 128 if dtype == "bf16" else 64
     inp = make_inputs(1, 2, N * c, D, seed=31, dtype=dtype)
@@ -105,7 +105,7 @@ def test_chained_steps_32_blocks_float32_state(ra, layout):
 
 
 @pytest.mark.parametrize("layout,causal", [("contiguous", True), ("striped", True), ("striped", False)])
-def test_fold_chain_32_blocks(ra, layout, causal):
+def test_fold_chain_32_blocks(ra, fwd_kernel, layout, causal):
     """ra_fwd_step_fold: every host folds its 32 rounds, in ring order, into a
     float32 state inside the forward epilogue; the state equals the oracle's
     rows at the forward's tolerance, and agrees with the step + merge chain."""
