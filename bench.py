@@ -55,9 +55,9 @@ UNIT = "TFLOP/s"
 # code it was taken on: the hash of csrc/<file> without comments (_src_hash)
 # at capture time.
 NCU_TRAFFIC = {
-    "fwd": {"sha256": "045f5236731c288193c86cecf3fb9a472a9b659f54307f603a3ffdb7d892ee9a", "workload": "long_128k", "bytes_per_launch": (19.252 + 1.185) * 1e9},
-    "bwd_dkv": {"sha256": "d03ea06215ec696de34c38fc93a4a393d6bdc5cc52cdd0f6c1718dbe747535dd", "workload": "long_128k", "bytes_per_launch": (12.889 + 2.137) * 1e9},
-    "bwd_dq": {"sha256": "d03ea06215ec696de34c38fc93a4a393d6bdc5cc52cdd0f6c1718dbe747535dd", "workload": "long_128k", "bytes_per_launch": (9.834 + 1.070) * 1e9},
+    "fwd": {"sha256": "1fd5226c09e127fc8c79982b484ebfac63235d7d37dc23198ff8717179c4c3e4", "workload": "long_128k", "bytes_per_launch": (17.237 + 1.218) * 1e9},
+    "bwd_dkv": {"sha256": "2cd114dc083486b62a781ff2c5c5b85003f5c222d07ef62ba0a8939e8e86990d", "workload": "long_128k", "bytes_per_launch": (11.253 + 2.136) * 1e9},
+    "bwd_dq": {"sha256": "2cd114dc083486b62a781ff2c5c5b85003f5c222d07ef62ba0a8939e8e86990d", "workload": "long_128k", "bytes_per_launch": (8.710 + 1.069) * 1e9},
     "decode_split": {"sha256": "db519d009c6e14d06bbde7b8df9ec6dab5ec5aeb1dc7cbff5fa4dc7eeea7a5b8", "workload": "decode_256k", "bytes_per_launch": 4295068000 + 6642688},
     "ffn_up": {"sha256": "e3c1fddde6a2bcd126b3ceb1de1f6d6f977d1cc7e45d80e1a639318de4a2afb1", "workload": "ffn_7b", "bytes_per_launch": (218.333 + 79.864) * 1e6},
 }
