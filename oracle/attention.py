@@ -293,6 +293,34 @@ def attention_bwd_head(q, k, v, o, lse, do, n_blocks: int, causal: bool, layout:
     return dQ, dK, dV
 
 
+def attention_bwd_head_chunked(q, k, v, o, lse, do, n_blocks: int, causal: bool, layout: str,
+                               row_chunk: int = 256):
+    """``attention_bwd_head`` for sequences whose S x S matrix of
+    probabilities does not fit in memory (ONE head; float64 [S, D], lse [S]).
+
+    The query rows are taken ``row_chunk`` at a time.  A chunk's rows of dQ
+    depend on that chunk alone; its contributions to dK and dV are added up
+    over the chunks, as dK_j and dV_j accumulate one query block per ring
+    round ([CH] §5.2).  Same formulas as ``attention_bwd_head``:
+        dV += P_c^T dO_c,  dS_c = P_c * (dO_c V^T - rowsum(dO_c * O_c)),
+        dQ_c = dS_c K / sqrt(D),  dK += dS_c^T Q_c / sqrt(D).
+    """
+    S, D = q.shape
+    dQ = np.zeros((S, D))
+    dK = np.zeros((S, D))
+    dV = np.zeros((S, D))
+    for r0 in range(0, S, row_chunk):
+        rows = np.arange(r0, min(S, r0 + row_chunk))
+        P = _probabilities(q, k, lse, n_blocks, causal, layout, rows=rows)
+        dV += P.T @ do[rows]
+        dP = do[rows] @ v.T
+        Dvec = (do[rows] * o[rows]).sum(axis=1)
+        dS = P * (dP - Dvec[:, None])
+        dQ[rows] = (dS @ k) / np.sqrt(D)
+        dK += (dS.T @ q[rows]) / np.sqrt(D)
+    return dQ, dK, dV
+
+
 def block_pair_bwd(q, k, v, o, lse, do, i: int, j: int, n_blocks: int, causal: bool, layout: str):
     """One ring round of the backward, ONE head: the contributions of query
     block i against KV block j alone.

@@ -308,8 +308,12 @@ def test_backward_matches_finite_differences(layout, causal):
     q, k, v, do = (_rand(rng, 1, 1, S, D) for _ in range(4))
     o, lse = orc.naive_attention(q, k, v, N, causal, layout)
     dq, dk, dv = orc.attention_bwd(q, k, v, o, lse, do, N, causal, layout)
+    # the chunked form (query rows 5 at a time: a ragged last chunk) is pinned the same way
+    cq, ck, cv = orc.attention_bwd_head_chunked(q[0, 0], k[0, 0], v[0, 0], o[0, 0], lse[0, 0], do[0, 0], N, causal,
+                                                layout, row_chunk=5)
     h = 1e-6
-    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv), ("q", q, cq[None, None]), ("k", k, ck[None, None]),
+                       ("v", v, cv[None, None])):
         num = np.zeros_like(x)
         for idx in np.ndindex(x.shape):
             xp, xm = x.copy(), x.copy()
@@ -335,6 +339,24 @@ def test_backward_sum_identities(layout):
     dq, dk, dv = orc.attention_bwd(q, k, v, o, lse, do, N, True, layout)
     np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
     np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("chunk", [1, 7, 64, 200])
+def test_chunked_backward_equals_whole_head(layout, causal, chunk):
+    """Taking the query rows a chunk at a time changes only the order of the
+    dK/dV sums (rounding), for chunks of one row, ragged chunks, and one chunk
+    larger than the sequence."""
+    rng = np.random.default_rng(52)
+    S, D, N = 64, 8, 4
+    q, k, v, do = (_rand(rng, S, D) for _ in range(4))
+    o, lse = orc.naive_attention(q[None, None], k[None, None], v[None, None], N, causal, layout)
+    o, lse = o[0, 0], lse[0, 0]
+    ref = orc.attention_bwd_head(q, k, v, o, lse, do, N, causal, layout)
+    got = orc.attention_bwd_head_chunked(q, k, v, o, lse, do, N, causal, layout, row_chunk=chunk)
+    for r, g in zip(ref, got):
+        np.testing.assert_allclose(g, r, rtol=1e-12, atol=1e-12)
 
 
 def test_dq_rows_match_full_backward():
