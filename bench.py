@@ -312,6 +312,30 @@ def _dist():
 
 
 # ----------------------------------------------------------------- CPU oracle
+def oracle_full(inp, w, with_bwd: bool):
+    """Time the whole oracle on the whole workload: every head, every row
+    (``naive_attention``) and, with the backward, ``attention_bwd_head_chunked``
+    on the oracle's own O and LSE.  One process; NumPy's BLAS uses the host
+    cores.  Returns (flops by the benchmark's convention, seconds, description)."""
+    import oracle as orc
+    B, H, S, D = inp["q"].shape
+    N, causal, layout = w["N"], w["causal"], w["layout"]
+    t0 = time.perf_counter()
+    for b in range(B):
+        for h in range(H):
+            q, k, v = (inp[x][b, h].double().numpy() for x in ("q", "k", "v"))
+            o, lse = orc.naive_attention(q[None, None], k[None, None], v[None, None], N, causal, layout,
+                                         row_chunk=128)
+            if with_bwd:
+                orc.attention_bwd_head_chunked(q, k, v, o[0, 0], lse[0, 0], inp["do"][b, h].double().numpy(), N,
+                                               causal, layout, row_chunk=128)
+    dt = time.perf_counter() - t0
+    from ring_attention_fwd_gb300 import flops as fl
+    f = fl.fwd_flops(B, H, S, D, causal) * (3.5 if with_bwd else 1.0)
+    return f, dt, (f"the whole workload: {B * H} heads, every row, forward" + (" and backward" if with_bwd else "")
+                   + ", float64")
+
+
 def oracle_sample(inp, w, budget_s: float):
     """Time the oracle on sampled query rows of one head (forward LSE/O and
     the dQ rows of the backward), growing the sample until `budget_s` is
@@ -573,8 +597,11 @@ def run_ours(args, w):
     }
     if rank == 0 and not args.no_cpu_baseline:
         cores = len(os.sched_getaffinity(0))
-        inp1 = {k: v[:1, :1] for k, v in inp.items()}
-        f, t, desc = oracle_sample(inp1, w, args.cpu_seconds)
+        if args.oracle_full:
+            f, t, desc = oracle_full(inp, w, with_bwd)
+        else:
+            inp1 = {k: v[:1, :1] for k, v in inp.items()}
+            f, t, desc = oracle_sample(inp1, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc + f"; {t:.1f} s of numpy float64"}
     if ws > 1:
@@ -964,6 +991,9 @@ def main():
                          "for profiling captures that must stay small)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="time the kernels only: no end-to-end copies, merge or CPU baseline (profiling runs)")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the oracle on the whole workload (every head and row) for cpu_baseline instead of "
+                         "a bounded sample; tens of minutes at 65536 tokens and beyond")
     ap.add_argument("--fwd-kernel", default="single", choices=["single", "pair"],
                     help="bf16 forward kernel: one CTA per SM (the library's default) or SM pairs")
     ap.add_argument("--balance", action="store_true",

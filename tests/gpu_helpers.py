@@ -47,6 +47,16 @@ def max_err(a, b) -> float:
     return float(np.nanmax(np.where(np.isnan(d), np.inf, d))) if d.size else 0.0
 
 
+def grad_errors(g, ref):
+    """(max |g - ref| / max(1, max |ref|), relative Frobenius error): the
+    backward's two figures, bounded by 2e-2 and 1e-2 for bf16."""
+    g = np.asarray(g, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = max(1.0, float(np.abs(ref).max()))
+    fro = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
+    return max_err(g, ref) / scale, fro
+
+
 def fwd_full_check(ra, inp: dict, N: int, causal: bool, layout: str, dtype: str):
     """Run the CUDA forward and compare every output with the oracle."""
     dev = to_cuda(inp)

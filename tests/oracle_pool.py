@@ -92,7 +92,39 @@ def _fwd_rows(paths, rows, N, causal, layout):
     return orc.attention_rows(_arr(paths["q"]), _arr(paths["k"]), _arr(paths["v"]), rows, N, causal, layout)
 
 
+def _full_head(paths, out_prefix, N, causal, layout, with_bwd, row_chunk):
+    import oracle as orc
+    q, k, v = (np.asarray(_arr(paths[x])) for x in ("q", "k", "v"))
+    o, lse = orc.naive_attention(q[None, None], k[None, None], v[None, None], N, causal, layout,
+                                 row_chunk=row_chunk)
+    res = {"o": o[0, 0], "lse": lse[0, 0]}
+    if with_bwd:
+        do = np.asarray(_arr(paths["do"]))
+        res["dq"], res["dk"], res["dv"] = orc.attention_bwd_head_chunked(q, k, v, res["o"], res["lse"], do, N,
+                                                                         causal, layout, row_chunk=row_chunk)
+    out = {}
+    for name, a in res.items():
+        out[name] = out_prefix + name + ".npy"
+        np.save(out[name], a)
+    return out
+
+
 # ------------------------------------------------------------------ parent API
+def full_heads(head_paths: list, N, causal, layout, with_bwd: bool, row_chunk: int = 256):
+    """The whole oracle of each head (``naive_attention`` over every row, and
+    ``attention_bwd_head_chunked`` if ``with_bwd``), one head per task, on
+    inputs shared with ``share``.  Yields (index, paths of the .npy results)
+    as heads finish; the caller releases both."""
+    global _dir
+    if _dir is None:
+        _dir = tempfile.mkdtemp(prefix="ra_oracle_")
+    futs = {pool().submit(_full_head, p, os.path.join(_dir, f"full{n}_"), N, causal, layout, with_bwd,
+                          row_chunk): n for n, p in enumerate(head_paths)}
+    for f in cf.as_completed(futs):
+        yield futs[f], f.result()
+
+
+
 def kv_rows(paths, keys, N, causal, layout, S, part_rows=2048):
     """``oracle.attention_bwd_kv_rows`` for ``keys``, its sum over query rows
     split into parts of ``part_rows`` rows run in parallel and added up."""
