@@ -150,14 +150,18 @@ def ring_backward(q, k, v, o, lse, do, *, causal: bool = True, layout: str = "co
     """Ring backward for this rank's blocks.
 
     q, k, v, o, do: this rank's blocks [B, H, c, D]; lse: its final [B, H, c]
-    LSE from the forward.  In round s the rank holds KV block j = (i - s) mod N
-    together with the float32 accumulators dK_j, dV_j that travelled with it;
-    it adds query block i's contributions (``step``) to its own dQ_i and to
-    dK_j, dV_j, then passes the four tensors on to rank i+1 (K_j, V_j are sent
-    while the round computes; the accumulators once it is done).  After the
-    last round the accumulators hop once more, which brings each rank's own
-    dK_i, dV_i home.  Contiguous causal rounds j > i add nothing and are
-    skipped (the data is still forwarded).
+    LSE from the forward.  In round s the rank holds KV block j = (i - s) mod N;
+    the float32 accumulators dK_j, dV_j travel the ring with it, one rank
+    behind: the rank adds query block i's contributions (``step``) to its own
+    dQ_i and to a zeroed partial of dK_j, dV_j, and only then waits for the
+    accumulators of block j from rank i-1, adds the partial into them and
+    passes them on to rank i+1.  K_j, V_j and the accumulators therefore both
+    move while the rounds compute.  After the last round the accumulators hop
+    once more, which brings each rank's own dK_i, dV_i home.  Contiguous causal
+    rounds j > i add nothing and are skipped (the data is still forwarded).
+    Per pair of ranks the transfers are posted in the same order on both sides
+    (K_j, V_j of round s, then the accumulators of round s), as point-to-point
+    backends match them by order.
     step(q, k_j, v_j, o, lse, do, dq, dk_j, dv_j, n, i, j) adds in place
     (default: the library's ``bwd_step``).  Returns float32 (dq, dk, dv)."""
     n = dist.get_world_size(group)
@@ -170,20 +174,37 @@ def ring_backward(q, k, v, o, lse, do, *, causal: bool = True, layout: str = "co
     send_to, recv_from = (i + 1) % n, (i - 1) % n
     f32 = dict(dtype=torch.float32, device=q.device)
     dq = torch.zeros(q.shape, **f32)
-    cur = [k, v, torch.zeros(k.shape, **f32), torch.zeros(v.shape, **f32)]
+    kv = [k, v]
+    sent = []                     # (requests, tensors) of the accumulators last passed on
     for s, j in enumerate(ring_order(i, n)):
+        acc, acc_reqs = None, []
+        if s > 0:                 # block j's accumulators from rank i-1, needed after this round's compute
+            acc = [torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)]
+            acc_reqs = dist.batch_isend_irecv([dist.P2POp(dist.irecv, acc[0], recv_from, group),
+                                               dist.P2POp(dist.irecv, acc[1], recv_from, group)])
         kv_reqs, nxt = [], None
-        if s < n - 1:       # K_j, V_j move on while this round computes
-            nxt = [torch.empty_like(cur[0]), torch.empty_like(cur[1])]
+        if s < n - 1:             # K_j, V_j move on while this round computes
+            nxt = [torch.empty_like(kv[0]), torch.empty_like(kv[1])]
             kv_reqs = dist.batch_isend_irecv([
-                dist.P2POp(dist.isend, cur[0], send_to, group), dist.P2POp(dist.irecv, nxt[0], recv_from, group),
-                dist.P2POp(dist.isend, cur[1], send_to, group), dist.P2POp(dist.irecv, nxt[1], recv_from, group)])
+                dist.P2POp(dist.isend, kv[0], send_to, group), dist.P2POp(dist.irecv, nxt[0], recv_from, group),
+                dist.P2POp(dist.isend, kv[1], send_to, group), dist.P2POp(dist.irecv, nxt[1], recv_from, group)])
+        part = [torch.zeros(k.shape, **f32), torch.zeros(v.shape, **f32)]
         if not (causal and layout == "contiguous" and j > i):
-            step(q, cur[0], cur[1], o, lse, do, dq, cur[2], cur[3], n, i, j)
-        acc = [torch.empty_like(cur[2]), torch.empty_like(cur[3])]
-        acc_reqs = dist.batch_isend_irecv([
-            dist.P2POp(dist.isend, cur[2], send_to, group), dist.P2POp(dist.irecv, acc[0], recv_from, group),
-            dist.P2POp(dist.isend, cur[3], send_to, group), dist.P2POp(dist.irecv, acc[1], recv_from, group)])
-        _wait_all(kv_reqs + acc_reqs, timeout_s, f"backward round {s} with ranks {recv_from}/{send_to}")
-        cur = (nxt or [None, None]) + acc
-    return dq, cur[2], cur[3]
+            step(q, kv[0], kv[1], o, lse, do, dq, part[0], part[1], n, i, j)
+        if acc is None:
+            acc = part
+        else:
+            _wait_all(acc_reqs, timeout_s, f"backward round {s}: accumulators from rank {recv_from}")
+            acc[0] += part[0]
+            acc[1] += part[1]
+        for reqs, _ in sent:
+            _wait_all(reqs, timeout_s, f"backward round {s}: accumulators to rank {send_to}")
+        sent = [(dist.batch_isend_irecv([dist.P2POp(dist.isend, acc[0], send_to, group),
+                                         dist.P2POp(dist.isend, acc[1], send_to, group)]), acc)]
+        _wait_all(kv_reqs, timeout_s, f"backward round {s} with ranks {recv_from}/{send_to}")
+        kv = nxt
+    home = [torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)]
+    reqs = dist.batch_isend_irecv([dist.P2POp(dist.irecv, home[0], recv_from, group),
+                                   dist.P2POp(dist.irecv, home[1], recv_from, group)])
+    _wait_all(reqs + sent[0][0], timeout_s, f"backward: own accumulators from rank {recv_from}")
+    return dq, home[0], home[1]

@@ -230,6 +230,8 @@ def _bwd_worker(rank, world, port, S, D, causal, layout, outdir, mode):
         def step(qq, kk, vv, oo, ll, dd, gq, gk, gv, n, i, j):
             assert torch.equal(kk, blk(k, j)) and torch.equal(vv, blk(v, j)), f"rank {i}: wrong block for {j}"
             assert gq.dtype == torch.float32 and gk.dtype == torch.float32
+            # the round adds into a fresh partial: it never waits for the accumulators in flight
+            assert not gk.any() and not gv.any(), f"rank {i}: round {j} got a non-zero dK/dV buffer"
             seen.append(j)
             a, b, cc = orc.block_pair_bwd(q, k, v, o, lse, do, i, j, n, causal, layout)
             gq[0, 0] += torch.from_numpy(a).float()
