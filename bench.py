@@ -514,8 +514,12 @@ def run_ours(args, w):
                        dv=y["dv"], workspace=work)
 
         e2e_steps = max(8, args.steps)          # amortises the unhidden first upload and last download
-        e2e_ms = pipelined_e2e(e2e_steps, stream, lambda b: [(ins[b][n], host[n]) for n in in_names], e2e_compute,
-                               lambda b: [(outs_host[n], outs[b][n]) for n in outs_host])
+        # The host link is shared with the machine's other GPUs and shows one-off stalls of 100-200 ms
+        # on a 4.3 GB copy: the pipelined loop runs three times and the median stands (all reported).
+        e2e_runs = [pipelined_e2e(e2e_steps, stream, lambda b: [(ins[b][n], host[n]) for n in in_names],
+                                  e2e_compute, lambda b: [(outs_host[n], outs[b][n]) for n in outs_host])
+                    for _ in range(3)]
+        e2e_ms = statistics.median(e2e_runs)
         link = link_times(stream, [(ins[1][n], host[n]) for n in in_names], [(outs_host[n], outs[0][n]) for n in outs_host])
         if ws > 1:
             tt = torch.tensor([e2e_ms], device="cuda")
@@ -585,6 +589,7 @@ def run_ours(args, w):
         "roofline": roofline,
         "e2e": ({"value": f_step * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                 "stat": "median of 3 runs", "ms_per_step_all": e2e_runs,
                  "copies": "overlapped with the neighbouring steps' compute on two copy streams (up, down); "
                            "double-buffered",
                  "link_alone": link} if e2e_ms is not None else None),
