@@ -55,7 +55,7 @@ UNIT = "TFLOP/s"
 # code it was taken on: the hash of csrc/<file> without comments (_src_hash)
 # at capture time.
 NCU_TRAFFIC = {
-    "fwd": {"sha256": "1fd5226c09e127fc8c79982b484ebfac63235d7d37dc23198ff8717179c4c3e4", "workload": "long_128k", "bytes_per_launch": (17.237 + 1.218) * 1e9},
+    "fwd": {"sha256": "a8b983f4ad109f5ccb021fb5f887f6e32dedae180da1253e95220a5374f1b78f", "workload": "long_128k", "bytes_per_launch": (27.160 + 1.250) * 1e9},
     "bwd_dkv": {"sha256": "2cd114dc083486b62a781ff2c5c5b85003f5c222d07ef62ba0a8939e8e86990d", "workload": "long_128k", "bytes_per_launch": (11.253 + 2.136) * 1e9},
     "bwd_dq": {"sha256": "2cd114dc083486b62a781ff2c5c5b85003f5c222d07ef62ba0a8939e8e86990d", "workload": "long_128k", "bytes_per_launch": (8.710 + 1.069) * 1e9},
     "decode_split": {"sha256": "db519d009c6e14d06bbde7b8df9ec6dab5ec5aeb1dc7cbff5fa4dc7eeea7a5b8", "workload": "decode_256k", "bytes_per_launch": 4295068000 + 6642688},
@@ -63,12 +63,15 @@ NCU_TRAFFIC = {
 }
 
 
-def _src_hash(name: str) -> str:
-    """SHA-256 of csrc/<name> with // comments and blank lines removed: the
-    recorded traffic stays valid across comment edits, not code changes."""
+def _src_hash(names) -> str:
+    """SHA-256 of csrc/<name> (or of several files, in order) with // comments
+    and blank lines removed: the recorded traffic stays valid across comment
+    edits, not code changes."""
     import re
-    with open(os.path.join(ROOT, "ring_attention_fwd_gb300", "csrc", name)) as f:
-        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
+    lines = []
+    for name in ([names] if isinstance(names, str) else names):
+        with open(os.path.join(ROOT, "ring_attention_fwd_gb300", "csrc", name)) as f:
+            lines += [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
     return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
 
 
@@ -558,8 +561,8 @@ def run_ours(args, w):
                 kernels[name]["per_clock_frac_at_smi_median"] = executed[name] / (cyc * sms * 8192)
     dom = max((n for n in kernels if n in algo), key=lambda n: kernels[n]["ms"])
     achieved = kernels[dom]["tflops_algorithmic"]
-    src_file = {"fwd": "fwd_bf16.cu", "fwd_pair": "fwd_bf16_pair.cu", "bwd_dkv": "bwd_bf16.cu",
-                "bwd_dq": "bwd_bf16.cu"}[dom]
+    src_file = {"fwd": ("fwd_bf16.cu", "fwd_softmax.cuh"), "fwd_pair": ("fwd_bf16_pair.cu", "fwd_softmax.cuh"),
+                "bwd_dkv": "bwd_bf16.cu", "bwd_dq": "bwd_bf16.cu"}[dom]
     tr = NCU_TRAFFIC.get(dom)
     traffic = tr["bytes_per_launch"] if tr and tr["sha256"] == _src_hash(src_file) and \
         tr["workload"] == args.workload and args.heads == 0 else None
