@@ -92,6 +92,16 @@ def test_balance_32k_full_forward_backward(ra, layout):
     _assert_within(worst, True)
 
 
+def test_batch2_noncausal_16k_full_forward_backward(ra):
+    """B = 2, 4 heads, 16384 tokens, 8 ring blocks, every key visible: the
+    unmasked path and the batch dimension, every element."""
+    w = dict(B=2, H=4, S=16384, D=128, N=8, causal=False, layout="contiguous", dtype="bf16", seed=16, scale=1.0,
+             grad=True)
+    worst, secs = _full_check(ra, w, w["layout"], True, 256)
+    print(f"batch 2 non-causal 16k full: {worst}, oracle {secs:.0f} s")
+    _assert_within(worst, True)
+
+
 @pytest.mark.skipif(not FULL, reason="oracle takes tens of minutes: set RA_FULL_PARITY=1")
 def test_fwdbwd_64k_full_forward_backward(ra):
     """65536 tokens, 32 heads, 16 ring blocks, causal striped: every element."""
