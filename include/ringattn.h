@@ -356,8 +356,9 @@ typedef struct {
   float ms;     /* duration, or -1 if it could not be measured */
   float sm_mhz; /* tensor-core kernels (bf16 forward, dK/dV, dQ): the SM clock
                    the kernel ran at, from its first CTA's cycle counter over
-                   its own lifetime against the global nanosecond timer;
-                   -1 for the other kernels */
+                   its own lifetime against the global nanosecond timer
+                   (kept for up to 256 such kernels between two reads; -1
+                   beyond that); -1 for the other kernels */
 } ra_kernel_time;
 RA_API int ra_set_kernel_timing(int enable);
 RA_API int ra_kernel_times(ra_kernel_time* out, int capacity, int* count);
